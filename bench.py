@@ -1,0 +1,383 @@
+#!/usr/bin/env python
+"""Benchmark of the dense joint text+image attention forward on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+One step = one dit_attn_forward over one batch of the workload (default: the
+2048x2048 text-to-image shape with its CFG batch, B=2 H=24 L=16896 d=128).
+Inputs are seeded synthetic bf16 tensors resident in HBM before timing; they
+total 595 MB, larger than the 126 MB L2, so no flush runs between steps.
+Timing: W untimed warm-up steps, then K steps bracketed by a barrier and a
+device synchronisation, CUDA events on the launching stream, max over ranks.
+Under torchrun every rank runs an independent replica of the workload on its
+own GPU (attention has no exchange step inside one layer), so scaling is weak.
+
+Rank 0 prints one JSON line.  `value` is TFLOP/s = 4*B*H*Lq*Lk*d / t summed
+over ranks; `e2e` is the same metric through the public API with pinned host
+buffers, host<->device copies inside the timed region; `roofline` relates the
+kernel's per-launch rate to the measured dense-bf16 peak; `cpu_baseline` times
+the FP64 oracle on a bounded sample of the same workload's query rows.
+
+--impl reference times the FP64 oracle (the only reference this method has)
+on the host cores, one bounded row sample per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention TFLOP/s (4·B·H·Lq·Lk·d/t) and % of B300 dense BF16 peak, 1 GPU"
+FALLBACK_PEAK_TFLOPS = 1800.0
+FALLBACK_SUSTAINED_TFLOPS = 1400.0
+FALLBACK_HBM_GBS = 6400.0
+KERNEL_SOURCES = ["diffusion_transformer_joint_causal_b300/csrc/dit_attn.cu",
+                  "diffusion_transformer_joint_causal_b300/csrc/ptx.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fmha_fwd_dram_traffic.txt")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="2048px_t2i_cfg")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target duration of the oracle's CPU-baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            m = json.load(f)
+        return {"bf16": float(m["bf16_tflops"]), "bf16_sustained": float(m["bf16_tflops_sustained"]),
+                "hbm": float(m["hbm_gbs"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"bf16": FALLBACK_PEAK_TFLOPS, "bf16_sustained": FALLBACK_SUSTAINED_TFLOPS,
+                "hbm": FALLBACK_HBM_GBS, "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha1()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from an ncu capture of this exact kernel source, else None."""
+    try:
+        src = kernel_source_hash()
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) >= 3 and not line.startswith("#") and parts[0] == src \
+                        and parts[1] == workload:
+                    return float(parts[2])
+    except OSError:
+        pass
+    return None
+
+
+class ClockSampler:
+    """Polls SM clock, power and clock-event reasons through NVML while running."""
+
+    REASONS = {  # NVML clocks-event reason bits
+        0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+        0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+        0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+        0x100: "display_clock_setting",
+    }
+
+    def __init__(self, device_index: int, period_s: float = 0.01):
+        self.samples = []
+        self.period = period_s
+        self.ok = False
+        self.max_mhz = None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception:
+            self.ok = False
+        self._stop = threading.Event()
+        self._t = None
+
+    def _reasons(self):
+        try:
+            return self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+        except Exception:
+            return self.nv.nvmlDeviceGetCurrentClocksThrottleReasons(self.h)
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append((self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM),
+                                     self._reasons()))
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def start(self):
+        if self.ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+
+    def stop(self):
+        if self._t:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"],
+                    "samples": 0}
+        mhz = [s[0] for s in self.samples]
+        bits = 0
+        for _, r in self.samples:
+            bits |= int(r)
+        reasons = [name for bit, name in self.REASONS.items() if bits & bit and name != "gpu_idle"]
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(mhz)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def oracle_sample(w, n_rows, n_threads):
+    """Time the FP64 oracle on the first n_rows of the workload's sampled query rows."""
+    import numpy as np
+
+    import oracle
+    import workloads as W
+    q, k, v = W.make_qkv(w)
+    bh, rows = [], []
+    for b in range(w.B):
+        for h in range(w.H):
+            r = W.sample_rows(w, b, h)
+            bh.append(np.full(r.shape, b * w.H + h))
+            rows.append(r)
+    bh, rows = np.concatenate(bh), np.concatenate(rows)
+    order = np.random.default_rng(0).permutation(len(rows))
+    bh, rows = bh[order], rows[order]
+
+    def run(n):
+        n = min(n, len(rows))
+        t0 = time.perf_counter()
+        oracle.attention_rows(q, k, v, w.scale, bh[:n], rows[:n], n_threads=n_threads)
+        return n, time.perf_counter() - t0
+
+    return run
+
+
+def cpu_baseline(w, seconds: float):
+    import oracle
+    threads = oracle.default_threads()
+    run = oracle_sample(w, 0, threads)
+    n1, t1 = run(threads)                       # calibration: one row per thread
+    n = max(threads, int(threads * seconds / max(t1, 1e-3)))
+    n, t = run(n)
+    flops = 4.0 * w.Lk * w.d * n
+    return {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} query rows of {w.name} (seeded 256-row samples per (b,h)), "
+                      f"FP64 C loop, {t:.1f} s"}
+
+
+def bench_reference(args):
+    import workloads as W
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    w = W.workload(args.workload)
+    threads = oracle.default_threads()
+    run = oracle_sample(w, 0, threads)
+    n1, t1 = run(threads)
+    # whole run within about two minutes: at most 2 s per step
+    step_s = min(2.0, 120.0 / max(1, args.steps + args.warmup))
+    per_step = max(threads, int(threads * step_s / max(t1, 1e-3)))
+    for _ in range(args.warmup):
+        run(per_step)
+    times = []
+    n_done = 0
+    for _ in range(args.steps):
+        n, t = run(per_step)
+        times.append(t)
+        n_done += n
+    total = sum(times)
+    value = 4.0 * w.Lk * w.d * n_done / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Lq": w.Lq, "Lk": w.Lk, "d": w.d,
+                   "rows_per_step": per_step},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{per_step} query rows of {w.name} per step, FP64 C loop"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def bench_ours(args):
+    import numpy as np
+    import torch
+
+    import diffusion_transformer_joint_causal_b300 as dit
+    import workloads as W
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dit.create()
+    w = W.workload(args.workload)
+    peaks = load_peaks()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as tdist
+            tdist.barrier()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        import torch.distributed as tdist
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        return float(t.item())
+
+    qb, kb, vb = W.make_qkv(w)
+    host = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in (qb, kb, vb)]
+    del qb, kb, vb
+    q, k, v = (t.to(dev) for t in host)
+    out = torch.empty_like(q)
+    stream = torch.cuda.current_stream(dev)
+    flops = w.flops
+
+    # ---- device-resident timing
+    for _ in range(max(args.warmup, 3)):
+        dit.forward(q, k, v, w.scale, out=out)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(local)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    ev[0].record(stream)
+    for i in range(args.steps):
+        dit.forward(q, k, v, w.scale, out=out)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    sampler.stop()
+    barrier()
+    per_launch = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[args.steps])
+    max_ms = max_over_ranks(total_ms)
+    value = world * flops * args.steps / (max_ms / 1e3) / 1e12
+    if dit.get_device_error() != 0:
+        raise RuntimeError("device-side wait timed out during the benchmark")
+
+    # ---- end to end through the public API with host buffers
+    out_host = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        qd = host[0].to(dev, non_blocking=True)
+        kd = host[1].to(dev, non_blocking=True)
+        vd = host[2].to(dev, non_blocking=True)
+        o = dit.forward(qd, kd, vd, w.scale)
+        out_host.copy_(o, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1))
+    e2e_value = world * flops * args.e2e_steps / (e2e_ms / 1e3) / 1e12
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as tdist
+            tdist.destroy_process_group()
+        return 0
+
+    mean_launch = statistics.mean(per_launch)
+    achieved = flops / (mean_launch / 1e3) / 1e12
+    traffic = recorded_traffic(w.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Lq": w.Lq, "Lk": w.Lk, "d": w.d,
+                   "segments": dict(w.segments), "parallelism": f"replicas x{world}",
+                   "l2": "inputs 595 MB > 126 MB L2, no flush between steps"
+                   if w.name == "2048px_t2i_cfg" else "see workload sizes"},
+        "pct_of_peak": 100.0 * value / world / peaks["bf16"],
+        "pct_of_sustained_peak": 100.0 * value / world / peaks["bf16_sustained"],
+        "ms_per_launch": {"mean": mean_launch, "median": statistics.median(per_launch),
+                          "min": min(per_launch)},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"],
+                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16"], "traffic": traffic,
+                     "peak_source": f"{peaks['source']} dense bf16 burst",
+                     "algorithmic_bytes": 2.0 * (2 * w.B * w.H * w.Lq * w.d
+                                                 + 2 * w.B * w.H * w.Lk * w.d),
+                     "kernel_source": kernel_source_hash()},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": sampler.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return bench_reference(args)
+    return bench_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

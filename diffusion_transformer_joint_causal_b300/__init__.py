@@ -1,0 +1,158 @@
+"""Python binding of the dit_attn C-ABI library (argument marshalling only).
+
+Every step of the attention forward runs in the CUDA kernels of
+``libdit_attn.so``; this module only checks tensors, passes their device
+pointers and the current CUDA stream through ctypes, and turns status codes
+into exceptions.  PyTorch supplies device memory and streams.  There is no
+fallback: if the library is missing, importing the names below raises.
+
+    import diffusion_transformer_joint_causal_b300 as dit
+    dit.create()                      # once per device
+    out = dit.forward(q, k, v)        # q,k,v: bf16 CUDA tensors [B, H, L, d]
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+__all__ = ["create", "destroy", "forward", "forward_ptr", "status_string", "get_device_error",
+           "last_cuda_error", "version", "library_path", "DitAttnError", "STATUS",
+           "EXPORTED_SYMBOLS"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libdit_attn.so")
+
+STATUS = {
+    0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "NOT_INITIALIZED",
+    4: "NO_DEVICE", 5: "CUDA", 6: "TIMEOUT",
+}
+
+EXPORTED_SYMBOLS = ("dit_attn_version", "dit_attn_create", "dit_attn_forward",
+                    "dit_attn_destroy", "dit_attn_status_string", "dit_attn_get_device_error",
+                    "dit_attn_last_cuda_error")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class DitAttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)} ({status_string(status)})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise ImportError(
+                    f"{_LIB_PATH} is missing; build it with "
+                    "`python -m diffusion_transformer_joint_causal_b300.build`")
+            lib = ctypes.CDLL(_LIB_PATH)
+            c_int, vp = ctypes.c_int, ctypes.c_void_p
+            lib.dit_attn_version.restype = c_int
+            lib.dit_attn_version.argtypes = []
+            lib.dit_attn_create.restype = c_int
+            lib.dit_attn_create.argtypes = []
+            lib.dit_attn_destroy.restype = c_int
+            lib.dit_attn_destroy.argtypes = []
+            lib.dit_attn_forward.restype = c_int
+            lib.dit_attn_forward.argtypes = [vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int,
+                                             ctypes.c_float, vp]
+            lib.dit_attn_status_string.restype = ctypes.c_char_p
+            lib.dit_attn_status_string.argtypes = [c_int]
+            lib.dit_attn_get_device_error.restype = c_int
+            lib.dit_attn_get_device_error.argtypes = [vp]
+            lib.dit_attn_last_cuda_error.restype = c_int
+            lib.dit_attn_last_cuda_error.argtypes = []
+            _lib = lib
+    return _lib
+
+
+def version() -> int:
+    return _load().dit_attn_version()
+
+
+def status_string(status: int) -> str:
+    return _load().dit_attn_status_string(int(status)).decode()
+
+
+def last_cuda_error() -> int:
+    return _load().dit_attn_last_cuda_error()
+
+
+def create() -> None:
+    """Prepare the current CUDA device (idempotent)."""
+    rc = _load().dit_attn_create()
+    if rc:
+        raise DitAttnError(rc, "dit_attn_create")
+
+
+def destroy() -> None:
+    rc = _load().dit_attn_destroy()
+    if rc:
+        raise DitAttnError(rc, "dit_attn_destroy")
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def get_device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the kernels' error word."""
+    return _load().dit_attn_get_device_error(_stream_handle(stream))
+
+
+def forward_ptr(q: int, k: int, v: int, out: int, B: int, H: int, Lq: int, Lk: int, d: int,
+                scale: float, stream=0) -> int:
+    """Raw C-ABI call with integer device pointers; returns the status code."""
+    s = stream if isinstance(stream, ctypes.c_void_p) else ctypes.c_void_p(int(stream))
+    return _load().dit_attn_forward(ctypes.c_void_p(q), ctypes.c_void_p(k), ctypes.c_void_p(v),
+                                    ctypes.c_void_p(out), B, H, Lq, Lk, d,
+                                    ctypes.c_float(scale), s)
+
+
+def forward(q, k, v, scale: float | None = None, out=None, stream=None):
+    """out = softmax(q k^T * scale) v over every (batch, head); bf16 in and out.
+
+    q: [B, H, Lq, d], k and v: [B, H, Lk, d], contiguous bf16 CUDA tensors on
+    one device; d is 64 or 128; scale defaults to 1/sqrt(d).  Enqueued on
+    ``stream`` (default: torch's current stream); returns ``out``.
+    """
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError(f"{name} must be a bfloat16 CUDA tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [B, H, L, d] tensor")
+    B, H, Lq, d = q.shape
+    Lk = k.shape[2]
+    if tuple(k.shape) != (B, H, Lk, d) or tuple(v.shape) != (B, H, Lk, d):
+        raise ValueError("k and v must be [B, H, Lk, d] with q's B, H and d")
+    if not (q.device == k.device == v.device):
+        raise ValueError("q, k, v must be on one device")
+    if out is None:
+        out = torch.empty_like(q)
+    elif (out.dtype != torch.bfloat16 or tuple(out.shape) != tuple(q.shape)
+          or not out.is_contiguous() or out.device != q.device):
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    with torch.cuda.device(q.device):
+        rc = forward_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                         B, H, Lq, Lk, d, float(scale), _stream_handle(stream))
+    if rc:
+        raise DitAttnError(rc, "dit_attn_forward")
+    return out

@@ -1,0 +1,684 @@
+// dit_attn: dense non-causal softmax attention forward for sm_103a (B300).
+//
+// Operation (standard attention, the baseline "traditional BF16 attention" of
+// "Speed Up Image Generation with FLUX 3 Image Klein on NVIDIA Blackwell
+// GPUs", attention paragraph): o_i = sum_j softmax_j(scale * q_i . k_j) v_j
+// for every (batch, head), over the joint text+image token sequence.
+//
+// Kernel structure (one persistent CTA per SM, 320 threads):
+//   warps 0-3  softmax warpgroup 0: owns query tile 0 (TMEM lanes 0..127)
+//   warps 4-7  softmax warpgroup 1: owns query tile 1
+//   warp  8    tcgen05 MMA issuer and TMEM allocator
+//   warp  9    TMA producer
+//   warps 10-11 idle (they complete the third warpgroup for setmaxnreg)
+// A work unit is 2 x 128 query rows of one (b,h).  Q tiles stay in shared
+// memory for the whole unit; K and V tiles of 128 keys stream through a ring
+// of shared-memory stages.  For every key tile j the MMA warp computes
+// S_t = Q_t K_j^T into TMEM; softmax warpgroup t turns S_t into bf16
+// probabilities P_t in place (the same TMEM columns), and the MMA warp then
+// accumulates O_t += P_t V_j in TMEM.  The two warpgroups alternate so that
+// one tile's softmax overlaps the other tile's MMAs.
+//
+// Online softmax (base 2): x = s * scale*log2(e); the running maximum m is
+// only raised when a tile's maximum exceeds it by more than 8 (a factor 256),
+// and then l and O are rescaled by exp2(m_old - m_new).  Probabilities are
+// exp2(x - m) <= 256, the row sum l accumulates in fp32, and the result
+// O / l is exact in exact arithmetic whatever m is.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/dit_attn.h"
+#include "ptx.cuh"
+
+namespace dit {
+
+// Set (never cleared by kernels) when a bounded wait gives up.
+__device__ int g_device_error = 0;
+
+constexpr int kBM = 128;                 // query rows per tile (one TMEM lane each)
+constexpr int kBN = 128;                 // keys per K/V tile
+constexpr int kTilesPerUnit = 2;         // query tiles per work unit
+constexpr int kUnitRows = kBM * kTilesPerUnit;
+constexpr int kNumThreads = 384;       // three full warpgroups (setmaxnreg works per warpgroup)
+// Register split: launched at 168 per thread (384 x 168 = 64512); the two
+// softmax warpgroups raise to 224 and the MMA/TMA warpgroup drops to 56:
+// 256 x 224 + 128 x 56 = 64512, exactly the launch's total.
+constexpr int kRegsSoftmax = 224;
+constexpr int kRegsOther = 56;
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s per wait
+constexpr float kRescaleThreshold = 8.0f;          // log2 units
+
+template <int D>
+struct Traits {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kBoxCols = 64;                         // one 128-byte swizzle span
+  static constexpr int kBoxes = D / kBoxCols;
+  static constexpr uint32_t kBoxBytes = 128u * 128u;          // 128 rows x 128 bytes
+  static constexpr uint32_t kTileBytes = kBoxBytes * kBoxes;  // one Q, K or V tile
+  static constexpr int kStages = D == 128 ? 4 : 8;
+  // TMEM columns (fp32): S0, S1, O0, O1.  P_t (bf16 pairs) reuses S_t's first 64.
+  __host__ __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
+  __host__ __device__ static constexpr uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(D) * t; }
+  static constexpr uint32_t kTmemCols = 512;
+  // shared memory (offsets from a 1024-byte aligned base)
+  static constexpr uint32_t kOffQ = 0;
+  static constexpr uint32_t kOffKV = kTilesPerUnit * kTileBytes;
+  static constexpr uint32_t kOffBar = kOffKV + kStages * kTileBytes;
+  // barriers: full[S], empty[S], q_full[2], q_empty[2], s_full[2], p_full[2], o_full[2], drain
+  static constexpr int kBarFull = 0;
+  static constexpr int kBarEmpty = kStages;
+  static constexpr int kBarQFull = 2 * kStages;
+  static constexpr int kBarQEmpty = kBarQFull + 2;
+  static constexpr int kBarSFull = kBarQEmpty + 2;
+  static constexpr int kBarPFull = kBarSFull + 2;
+  static constexpr int kBarOFull = kBarPFull + 2;
+  static constexpr int kBarDrain = kBarOFull + 2;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr uint32_t kSmemBytes = 1024 + kOffMisc + 16;
+};
+
+struct Params {
+  __nv_bfloat16* out;
+  int Lq, Lk;
+  int num_qblocks;   // ceil(Lq / 256)
+  int num_units;     // B*H*num_qblocks
+  float scale_log2;  // scale * log2(e)
+};
+
+struct Shared {
+  uint32_t base;          // shared-window address of the aligned base
+  uint32_t bar0;          // address of barrier 0
+  volatile int* abort;    // set when any role gives up
+  __device__ uint32_t bar(int i) const { return bar0 + 8u * static_cast<uint32_t>(i); }
+};
+
+__device__ __forceinline__ void record_timeout(const Shared& sh) {
+  *sh.abort = 1;
+  atomicExch(&g_device_error, DIT_ATTN_ERR_TIMEOUT);
+}
+
+// ----------------------------------------------------------------- producer
+template <int D>
+__device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                          const Params& p, const Shared& sh) {
+  using T = Traits<D>;
+  const uint64_t pol_kv = policy_evict_last();
+  const uint64_t pol_q = policy_evict_first();
+  uint32_t stage = 0, phase = 0;
+  uint32_t n_fills = 0;                  // K/V fills issued (saturates at kStages)
+  uint32_t q_fills = 0;                  // bit t: query tile t was ever loaded
+  uint32_t q_parity = 0;                 // bit t: parity of tile t's last load
+  bool ok = true;
+  const int n_kv = (p.Lk + kBN - 1) / kBN;
+  uint32_t it = 0;
+
+  auto load_q = [&](int t, int bh, int row0) -> bool {
+    if (!mbar_wait(sh.bar(T::kBarQEmpty + t), (it & 1u) ^ 1u, kWaitLimitNs, sh.abort)) return false;
+    const uint32_t bar = sh.bar(T::kBarQFull + t);
+    mbar_arrive_expect_tx(bar, T::kTileBytes);
+    const uint32_t dst = sh.base + T::kOffQ + t * T::kTileBytes;
+    for (int b = 0; b < T::kBoxes; ++b)
+      tma_load_3d(dst + b * T::kBoxBytes, tmQ, bar, b * T::kBoxCols, row0 + t * kBM, bh, pol_q);
+    q_fills |= 1u << t;
+    q_parity = (q_parity & ~(1u << t)) | ((it & 1u) << t);
+    return true;
+  };
+  auto load_kv = [&](const CUtensorMap* tm, int bh, int key0) -> bool {
+    if (!mbar_wait(sh.bar(T::kBarEmpty + stage), phase ^ 1u, kWaitLimitNs, sh.abort)) return false;
+    const uint32_t bar = sh.bar(T::kBarFull + stage);
+    mbar_arrive_expect_tx(bar, T::kTileBytes);
+    const uint32_t dst = sh.base + T::kOffKV + stage * T::kTileBytes;
+    for (int b = 0; b < T::kBoxes; ++b)
+      tma_load_3d(dst + b * T::kBoxBytes, tm, bar, b * T::kBoxCols, key0, bh, pol_kv);
+    if (n_fills < T::kStages) ++n_fills;
+    if (++stage == T::kStages) { stage = 0; phase ^= 1u; }
+    return true;
+  };
+
+  for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++it) {
+    const int bh = u / p.num_qblocks;
+    const int row0 = (u % p.num_qblocks) * kUnitRows;
+    ok = load_q(0, bh, row0);
+    for (int j = 0; j < n_kv && ok; ++j) {
+      ok = load_kv(tmK, bh, j * kBN);
+      if (ok && j == 0) ok = load_q(1, bh, row0);
+      if (ok) ok = load_kv(tmV, bh, j * kBN);
+    }
+  }
+  if (!ok) {
+    record_timeout(sh);
+    // Let every copy already issued land before the CTA's shared memory goes away.
+    const volatile int no_abort = 0;
+    // The last n_fills fills went to the stages just before `stage`.
+    uint32_t s = stage, ph = phase;
+    for (uint32_t f = 0; f < n_fills; ++f) {
+      if (s == 0) { s = T::kStages - 1; ph ^= 1u; } else { --s; }
+      mbar_wait(sh.bar(T::kBarFull + s), ph, kWaitLimitNs, &no_abort);
+    }
+    for (int t = 0; t < 2; ++t)
+      if (q_fills & (1u << t))
+        mbar_wait(sh.bar(T::kBarQFull + t), (q_parity >> t) & 1u, kWaitLimitNs, &no_abort);
+  }
+}
+
+// ----------------------------------------------------------------- MMA issuer
+// The 14-bit start-address field of a descriptor holds (address >> 4); the
+// shared window is below 256 KB, so adding (bytes >> 4) to the descriptor
+// advances the start address without touching other fields.
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+  using T = Traits<D>;
+  constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, 0, 0);
+  const uint64_t qd = smem_desc_sw128(q_smem, 16, 1024);
+  const uint64_t kd = smem_desc_sw128(k_smem, 16, 1024);
+#pragma unroll 1
+  for (int k = 0; k < D / 16; ++k) {
+    // K step k: 16 columns = 32 bytes into the 128-byte swizzle span, box k/4.
+    const uint64_t off = ((k / 4) * T::kBoxBytes + (k % 4) * 32) >> 4;
+    mma_ss(d_tmem, qd + off, kd + off, idesc, k > 0 ? 1u : 0u);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
+                                         bool accumulate) {
+  using T = Traits<D>;
+  constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, 0, 1);
+  // V is [keys][d] with d contiguous: the B operand in MN-major form.  The
+  // second 64-column box is LBO away; 8-key row groups are SBO = 1024 apart.
+  const uint64_t vd = smem_desc_sw128(v_smem, T::kBoxBytes, 1024);
+#pragma unroll 1
+  for (int k = 0; k < kBN / 16; ++k) {
+    // K step k: 16 keys = 16 rows of 128 bytes; P columns hold bf16 pairs.
+    mma_ts(d_tmem, p_tmem + k * 8, vd + ((k * 16 * 128) >> 4), idesc,
+           (accumulate || k > 0) ? 1u : 0u);
+  }
+}
+
+template <int D>
+__device__ void mma_role(const Params& p, const Shared& sh, uint32_t tmem) {
+  using T = Traits<D>;
+  uint32_t stage = 0, phase = 0;
+  uint32_t g = 0;    // key-tile iterations so far (P hand-offs per query tile)
+  uint32_t it = 0;   // work units so far
+  bool ok = true;
+  const int n_kv = (p.Lk + kBN - 1) / kBN;
+  const uint32_t q_smem[2] = {sh.base + T::kOffQ, sh.base + T::kOffQ + T::kTileBytes};
+  auto kv_smem = [&](uint32_t s) { return sh.base + T::kOffKV + s * T::kTileBytes; };
+  auto take_stage = [&](uint32_t& s_out) -> bool {
+    s_out = stage;
+    if (!mbar_wait(sh.bar(T::kBarFull + stage), phase, kWaitLimitNs, sh.abort)) return false;
+    if (++stage == T::kStages) { stage = 0; phase ^= 1u; }
+    return true;
+  };
+
+  for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++it) {
+    uint32_t sK = 0, sV = 0;
+    // S_t = Q_t K_0^T for both tiles
+    ok = mbar_wait(sh.bar(T::kBarQFull + 0), it & 1u, kWaitLimitNs, sh.abort) && take_stage(sK);
+    if (!ok) break;
+    tc_fence_after();
+    issue_qk<D>(tmem + T::col_s(0), q_smem[0], kv_smem(sK));
+    mma_commit(sh.bar(T::kBarSFull + 0));
+    if (n_kv == 1) mma_commit(sh.bar(T::kBarQEmpty + 0));
+    ok = mbar_wait(sh.bar(T::kBarQFull + 1), it & 1u, kWaitLimitNs, sh.abort);
+    if (!ok) break;
+    tc_fence_after();
+    issue_qk<D>(tmem + T::col_s(1), q_smem[1], kv_smem(sK));
+    mma_commit(sh.bar(T::kBarSFull + 1));
+    if (n_kv == 1) mma_commit(sh.bar(T::kBarQEmpty + 1));
+    mma_commit(sh.bar(T::kBarEmpty + sK));
+
+    for (int j = 0; j < n_kv && ok; ++j, ++g) {
+      const bool more = j + 1 < n_kv;
+      ok = take_stage(sV) && mbar_wait(sh.bar(T::kBarPFull + 0), g & 1u, kWaitLimitNs, sh.abort);
+      if (!ok) break;
+      tc_fence_after();
+      issue_pv<D>(tmem + T::col_o(0), tmem + T::col_s(0), kv_smem(sV), j > 0);
+      if (more) {
+        ok = take_stage(sK);
+        if (!ok) break;
+        tc_fence_after();
+        issue_qk<D>(tmem + T::col_s(0), q_smem[0], kv_smem(sK));
+        mma_commit(sh.bar(T::kBarSFull + 0));
+        if (j + 2 == n_kv) mma_commit(sh.bar(T::kBarQEmpty + 0));
+      } else {
+        mma_commit(sh.bar(T::kBarOFull + 0));
+      }
+      ok = mbar_wait(sh.bar(T::kBarPFull + 1), g & 1u, kWaitLimitNs, sh.abort);
+      if (!ok) break;
+      tc_fence_after();
+      issue_pv<D>(tmem + T::col_o(1), tmem + T::col_s(1), kv_smem(sV), j > 0);
+      mma_commit(sh.bar(T::kBarEmpty + sV));
+      if (more) {
+        issue_qk<D>(tmem + T::col_s(1), q_smem[1], kv_smem(sK));
+        mma_commit(sh.bar(T::kBarSFull + 1));
+        if (j + 2 == n_kv) mma_commit(sh.bar(T::kBarQEmpty + 1));
+        mma_commit(sh.bar(T::kBarEmpty + sK));
+      } else {
+        mma_commit(sh.bar(T::kBarOFull + 1));
+      }
+    }
+  }
+  if (!ok) record_timeout(sh);
+  // Drain: every MMA this thread issued completes before TMEM is released.
+  mma_commit(sh.bar(T::kBarDrain));
+  const volatile int no_abort = 0;
+  mbar_wait(sh.bar(T::kBarDrain), 0, kWaitLimitNs, &no_abort);
+}
+
+// ----------------------------------------------------------------- softmax + epilogue
+// One thread per query row: thread r of the warpgroup owns TMEM lane r.
+template <int D>
+__device__ __forceinline__ void rescale_o(uint32_t taddr_o, float factor) {
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t o[32];
+    tmem_ld32(taddr_o + c * 32, o);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * factor);
+    tmem_st32(taddr_o + c * 32, o);
+  }
+}
+
+// exp2 of one S tile into packed bf16 probabilities, written back over the
+// first 64 TMEM columns of S (each half as soon as it is packed).  Returns the
+// sum of the probabilities *as rounded to bf16*, so that the row sum l and the
+// P.V product weigh every key identically (a row dominated by one key then
+// returns that key's value row without a rounding-induced scale error).
+// kMasked: keys at or beyond `valid` get probability 0.
+template <bool kMasked>
+__device__ __forceinline__ float probs_tile(const uint32_t (&sr)[4][32], float scale_log2,
+                                            float neg_m, int valid, uint32_t taddr_p) {
+  const float2 sl2 = make_float2(scale_log2, scale_log2);
+  const float2 nm = make_float2(neg_m, neg_m);
+  float2 acc[4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) acc[a] = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    uint32_t pk[32];
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      const int c = 2 * h + cc;
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        const float2 x = __ffma2_rn(
+            make_float2(__uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1])), sl2, nm);
+        float p0 = ex2_approx(x.x);
+        float p1 = ex2_approx(x.y);
+        if (kMasked) {
+          p0 = (c * 32 + i < valid) ? p0 : 0.f;
+          p1 = (c * 32 + i + 1 < valid) ? p1 : 0.f;
+        }
+        const uint32_t w = pack_bf16x2(p0, p1);
+        pk[cc * 16 + i / 2] = w;
+        acc[(i / 2) & 3] = __fadd2_rn(
+            acc[(i / 2) & 3], make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)));
+      }
+    }
+    tmem_st32(taddr_p + h * 32, pk);
+  }
+  const float2 s01 = __fadd2_rn(acc[0], acc[1]);
+  const float2 s23 = __fadd2_rn(acc[2], acc[3]);
+  const float2 s = __fadd2_rn(s01, s23);
+  return s.x + s.y;
+}
+
+template <bool kMasked>
+__device__ __forceinline__ float rowmax_tile(const uint32_t (&sr)[4][32], int valid) {
+  float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      float a = __uint_as_float(sr[c][i]), b = __uint_as_float(sr[c][i + 1]);
+      if (kMasked) {
+        a = (c * 32 + i < valid) ? a : -INFINITY;
+        b = (c * 32 + i + 1 < valid) ? b : -INFINITY;
+      }
+      m[(i / 2) & 3] = fmax3(m[(i / 2) & 3], a, b);
+    }
+  return fmax3(m[0], m[1], fmaxf(m[2], m[3]));
+}
+
+template <int D>
+__device__ void softmax_role(const Params& p, const Shared& sh, uint32_t tmem, int t) {
+  using T = Traits<D>;
+  const int wg_warp = (threadIdx.x / 32) & 3;
+  const int r = wg_warp * 32 + (threadIdx.x & 31);   // row within the query tile
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(wg_warp * 32) << 16);
+  const uint32_t taddr_s = lane_base + T::col_s(t);
+  const uint32_t taddr_o = lane_base + T::col_o(t);
+  const float scale_log2 = p.scale_log2;
+  const int n_kv = (p.Lk + kBN - 1) / kBN;
+  const int tail = p.Lk - (n_kv - 1) * kBN;   // valid keys in the last tile, 1..128
+  uint32_t g = 0, it = 0;
+  bool ok = true;
+
+  for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++it) {
+    const int bh = u / p.num_qblocks;
+    const int row = (u % p.num_qblocks) * kUnitRows + t * kBM + r;
+    float m_used = -INFINITY;   // running max, in units of s*scale*log2(e)
+    float l = 0.f;
+    for (int j = 0; j < n_kv; ++j, ++g) {
+      const bool got = mbar_wait(sh.bar(T::kBarSFull + t), g & 1u, kWaitLimitNs, sh.abort);
+      if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(taddr_s + c * 32, sr[c]);
+      tmem_wait_ld();
+      const bool masked = (j == n_kv - 1) && (tail < kBN);
+      const float mx = masked ? rowmax_tile<true>(sr, tail) : rowmax_tile<false>(sr, kBN);
+      const float m_tile = mx * scale_log2;
+      float factor = 1.f;
+      if (m_tile > m_used + kRescaleThreshold) {
+        factor = ex2_approx(m_used - m_tile);   // 0 on the first tile
+        l *= factor;
+        m_used = m_tile;
+      }
+      // O_t is quiescent here: S_t's completion implies the previous P.V product finished.
+      if (j > 0 && __any_sync(0xffffffffu, factor != 1.f)) rescale_o<D>(taddr_o, factor);
+      const float neg_m = -m_used;
+      l += masked ? probs_tile<true>(sr, scale_log2, neg_m, tail, taddr_s)
+                  : probs_tile<false>(sr, scale_log2, neg_m, kBN, taddr_s);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(sh.bar(T::kBarPFull + t));
+    }
+    if (!ok) break;
+    // Epilogue: O_t / l -> bf16 -> global, one contiguous row per thread.
+    const bool got = mbar_wait(sh.bar(T::kBarOFull + t), it & 1u, kWaitLimitNs, sh.abort);
+    if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+    tc_fence_after();
+    const float inv_l = 1.f / l;
+    const bool row_ok = row < p.Lq;
+    uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(bh) * p.Lq + row) * D);
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o[32];
+      tmem_ld32(taddr_o + c * 32, o);
+      tmem_wait_ld();
+      uint32_t w[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+      if (row_ok) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          dst[c * 4 + v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+      }
+    }
+  }
+  if (!ok) record_timeout(sh);
+}
+
+// ----------------------------------------------------------------- kernel
+template <int D>
+__global__ void __launch_bounds__(kNumThreads, 1)
+    fmha_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const Params p) {
+  using T = Traits<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(base_ptr + T::kOffMisc);  // [0] TMEM address, [1] abort
+  Shared sh;
+  sh.base = base;
+  sh.bar0 = base + T::kOffBar;
+  sh.abort = reinterpret_cast<volatile int*>(misc + 1);
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < T::kStages; ++s) {
+      mbar_init(sh.bar(T::kBarFull + s), 1);
+      mbar_init(sh.bar(T::kBarEmpty + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(sh.bar(T::kBarQFull + t), 1);
+      mbar_init(sh.bar(T::kBarQEmpty + t), 1);
+      mbar_init(sh.bar(T::kBarSFull + t), 1);
+      mbar_init(sh.bar(T::kBarPFull + t), kBM);
+      mbar_init(sh.bar(T::kBarOFull + t), 1);
+    }
+    mbar_init(sh.bar(T::kBarDrain), 1);
+    *sh.abort = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == kLoadWarp && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(misc), T::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+
+  if (warp < kMmaWarp) {
+    reg_alloc<kRegsSoftmax>();
+    softmax_role<D>(p, sh, tmem, warp / 4);
+  } else if (warp == kMmaWarp) {
+    reg_dealloc<kRegsOther>();
+    if (lane == 0) mma_role<D>(p, sh, tmem);
+    __syncwarp();
+  } else if (warp == kLoadWarp) {
+    reg_dealloc<kRegsOther>();
+    if (lane == 0) load_role<D>(&tmQ, &tmK, &tmV, p, sh);
+    __syncwarp();
+  } else {
+    reg_dealloc<kRegsOther>();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, T::kTmemCols);
+  }
+}
+
+}  // namespace dit
+
+// =================================================================== host side
+namespace {
+
+using dit::Traits;
+
+struct DeviceState {
+  bool ready = false;
+  int num_sms = 0;
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+DeviceState g_state[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+thread_local int g_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return DIT_ATTN_ERR_CUDA;
+}
+
+bool current_device(int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return *dev >= 0 && *dev < kMaxDevices;
+}
+
+// 3-D bf16 view [BH][L][d] with a 64-column x 128-row box and 128-byte swizzle.
+// Rows beyond L inside one head read as zeros, never as the next head's rows.
+int encode_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t L, int d) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(L),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(L) * static_cast<cuuint64_t>(d) * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    g_last_cuda_error = static_cast<int>(r);
+    return DIT_ATTN_ERR_CUDA;
+  }
+  return DIT_ATTN_OK;
+}
+
+bool overlaps(const void* a, int64_t a_bytes, const void* b, int64_t b_bytes) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + static_cast<uintptr_t>(b_bytes) && b0 < a0 + static_cast<uintptr_t>(a_bytes);
+}
+
+template <int D>
+int launch(const void* q, const void* k, const void* v, void* out, int64_t BH, int Lq, int Lk,
+           float scale, cudaStream_t stream, int num_sms) {
+  CUtensorMap tq, tk, tv;
+  int rc;
+  if ((rc = encode_map(&tq, q, BH, Lq, D)) != DIT_ATTN_OK) return rc;
+  if ((rc = encode_map(&tk, k, BH, Lk, D)) != DIT_ATTN_OK) return rc;
+  if ((rc = encode_map(&tv, v, BH, Lk, D)) != DIT_ATTN_OK) return rc;
+  dit::Params p;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.num_qblocks = (Lq + dit::kUnitRows - 1) / dit::kUnitRows;
+  p.num_units = static_cast<int>(BH * p.num_qblocks);
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  const int grid = p.num_units < num_sms ? p.num_units : num_sms;
+  dit::fmha_fwd_kernel<D><<<grid, dit::kNumThreads, Traits<D>::kSmemBytes, stream>>>(tq, tk, tv, p);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return DIT_ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dit_attn_version(void) { return 100; }
+
+const char* dit_attn_status_string(int status) {
+  switch (status) {
+    case DIT_ATTN_OK: return "ok";
+    case DIT_ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case DIT_ATTN_ERR_UNSUPPORTED: return "unsupported head dim or size";
+    case DIT_ATTN_ERR_NOT_INITIALIZED: return "dit_attn_create() not called for this device";
+    case DIT_ATTN_ERR_NO_DEVICE: return "no sm_103 CUDA device";
+    case DIT_ATTN_ERR_CUDA: return "CUDA error";
+    case DIT_ATTN_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int dit_attn_last_cuda_error(void) { return g_last_cuda_error; }
+
+int dit_attn_create(void) {
+  int dev = -1;
+  if (!current_device(&dev)) return DIT_ATTN_ERR_NO_DEVICE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_state[dev].ready) return DIT_ATTN_OK;
+  cudaDeviceProp prop;
+  cudaError_t e = cudaGetDeviceProperties(&prop, dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (prop.major != 10 || prop.minor != 3) return DIT_ATTN_ERR_NO_DEVICE;
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (q != cudaDriverEntryPointSuccess || !fn) return cuda_fail(cudaErrorSymbolNotFound);
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  e = cudaFuncSetAttribute(dit::fmha_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Traits<64>::kSmemBytes);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = cudaFuncSetAttribute(dit::fmha_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Traits<128>::kSmemBytes);
+  if (e != cudaSuccess) return cuda_fail(e);
+  g_state[dev].num_sms = prop.multiProcessorCount;
+  g_state[dev].ready = true;
+  return DIT_ATTN_OK;
+}
+
+int dit_attn_destroy(void) {
+  int dev = -1;
+  if (!current_device(&dev)) return DIT_ATTN_ERR_NO_DEVICE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_state[dev] = DeviceState();
+  return DIT_ATTN_OK;
+}
+
+int dit_attn_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int Lq,
+                     int Lk, int d, float scale, void* stream) {
+  if (!q || !k || !v || !out) return DIT_ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Lq < 1 || Lk < 1) return DIT_ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.f) return DIT_ATTN_ERR_INVALID_ARG;
+  const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out);
+  if (mis & 15u) return DIT_ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return DIT_ATTN_ERR_UNSUPPORTED;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  const int64_t qblocks = (static_cast<int64_t>(Lq) + dit::kUnitRows - 1) / dit::kUnitRows;
+  if (BH > INT_MAX || Lq > INT_MAX - 2 * dit::kUnitRows || Lk > INT_MAX - 2 * dit::kUnitRows ||
+      BH * qblocks > INT_MAX)
+    return DIT_ATTN_ERR_UNSUPPORTED;
+  const int64_t q_bytes = BH * Lq * d * 2, kv_bytes = BH * Lk * d * 2;
+  if (overlaps(out, q_bytes, q, q_bytes) || overlaps(out, q_bytes, k, kv_bytes) ||
+      overlaps(out, q_bytes, v, kv_bytes))
+    return DIT_ATTN_ERR_INVALID_ARG;
+
+  int dev = -1;
+  if (!current_device(&dev)) return DIT_ATTN_ERR_NO_DEVICE;
+  int num_sms;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_state[dev].ready) return DIT_ATTN_ERR_NOT_INITIALIZED;
+    num_sms = g_state[dev].num_sms;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return d == 64 ? launch<64>(q, k, v, out, BH, Lq, Lk, scale, s, num_sms)
+                 : launch<128>(q, k, v, out, BH, Lq, Lk, scale, s, num_sms);
+}
+
+int dit_attn_get_device_error(void* stream) {
+  int dev = -1;
+  if (!current_device(&dev)) return DIT_ATTN_ERR_NO_DEVICE;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  int word = 0;
+  e = cudaMemcpyFromSymbol(&word, dit::g_device_error, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (word != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(dit::g_device_error, &zero, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return word;
+  }
+  return DIT_ATTN_OK;
+}
+
+}  // extern "C"

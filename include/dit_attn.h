@@ -1,0 +1,96 @@
+/*
+ * dit_attn — dense, non-causal, multi-head softmax attention forward for the
+ * joint text+image token sequence of a diffusion transformer, on NVIDIA B300
+ * (sm_103a).
+ *
+ * The operation is standard attention, the "traditional / standard BF16
+ * attention" that "Speed Up Image Generation with FLUX 3 Image Klein on NVIDIA
+ * Blackwell GPUs" (attention paragraph; also the Japanese summary on
+ * sns.style, fourth paragraph) measures at about 60% of DiT kernel time at
+ * 2048x2048.  For every batch b, head h and query row i:
+ *
+ *     s_ij = scale * sum_c q[b,h,i,c] * k[b,h,j,c]        (j < Lk, no mask)
+ *     o[b,h,i,:] = sum_j softmax_j(s_ij) * v[b,h,j,:]
+ *
+ * The text, image and reference-image tokens of a DiT block form one
+ * sequence; every query sees every key.
+ *
+ * Tensors (all owned by the caller; the library never allocates per call):
+ *   q   : device pointer, bf16, contiguous [B, H, Lq, d]
+ *   k, v: device pointers, bf16, contiguous [B, H, Lk, d]
+ *   out : device pointer, bf16, contiguous [B, H, Lq, d]; written, never read
+ * Every pointer must be 16-byte aligned; out must not overlap q, k or v.
+ * d must be 64 or 128.  Arithmetic: bf16 tensor-core products with fp32
+ * accumulation, fp32 online softmax, probabilities rounded to bf16 before the
+ * P.V product, output rounded to nearest-even bf16.
+ *
+ * Streams: work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
+ * default stream).  No call synchronises, except dit_attn_get_device_error.
+ * Calls keep no per-call device state, so calls on different streams may
+ * overlap.
+ *
+ * Errors: every entry point returns a dit_attn_status.  Argument checks run
+ * before any CUDA call, so an invalid call has no side effect.
+ */
+#ifndef DIT_ATTN_H
+#define DIT_ATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dit_attn_status {
+  DIT_ATTN_OK = 0,
+  DIT_ATTN_ERR_INVALID_ARG = 1,     /* null / misaligned pointer, size < 1, bad scale, overlap */
+  DIT_ATTN_ERR_UNSUPPORTED = 2,     /* head dim other than 64 or 128; sizes beyond the limits */
+  DIT_ATTN_ERR_NOT_INITIALIZED = 3, /* dit_attn_create() not called for the current device */
+  DIT_ATTN_ERR_NO_DEVICE = 4,       /* no CUDA device, or the current device is not sm_103 */
+  DIT_ATTN_ERR_CUDA = 5,            /* a CUDA runtime/driver call failed; see dit_attn_last_cuda_error */
+  DIT_ATTN_ERR_TIMEOUT = 6          /* a kernel gave up a bounded wait (reported by get_device_error) */
+} dit_attn_status;
+
+/* Library version, e.g. 100 for 0.1.0. */
+int dit_attn_version(void);
+
+/*
+ * Prepare the current CUDA device: checks that it is compute capability 10.3,
+ * reads its SM count, raises the kernels' dynamic shared-memory limit and
+ * resolves the driver's tensor-map encoder.  Idempotent and thread-safe; call
+ * once per device before dit_attn_forward.  Returns NO_DEVICE when no usable
+ * device is present.
+ */
+int dit_attn_create(void);
+
+/*
+ * out = softmax(q k^T * scale) v for every (batch, head), enqueued on stream.
+ *   B, H, Lq, Lk >= 1; B*H*max(Lq,Lk)*d < 2^31; Lq, Lk < 2^31.
+ *   d in {64, 128}.
+ *   scale finite and >= 0 (1/sqrt(d) for a standard transformer).
+ * Asynchronous: returns after the launch.  A launch failure returns
+ * DIT_ATTN_ERR_CUDA; a device-side wait that gave up is reported later by
+ * dit_attn_get_device_error.
+ */
+int dit_attn_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int Lq,
+                     int Lk, int d, float scale, void* stream);
+
+/* Forget the current device's state; forward then returns NOT_INITIALIZED. */
+int dit_attn_destroy(void);
+
+/* Static, human-readable name of a status code. */
+const char* dit_attn_status_string(int status);
+
+/*
+ * Synchronise `stream`, then read and clear the device error word that the
+ * kernels set when a bounded wait gives up.  Returns OK or TIMEOUT (or CUDA
+ * if the synchronisation itself failed).  A test and debugging aid.
+ */
+int dit_attn_get_device_error(void* stream);
+
+/* The cudaError_t behind the most recent DIT_ATTN_ERR_CUDA on this thread. */
+int dit_attn_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DIT_ATTN_H */

@@ -1,0 +1,99 @@
+"""C-ABI library: loads, exports every declared entry point, validates arguments.
+
+These run without a GPU: argument checks happen before any CUDA call, so an
+invalid call returns its status code on any host, and a valid call on a host
+with no device returns NO_DEVICE instead of touching CUDA memory.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import diffusion_transformer_joint_causal_b300 as dit
+from diffusion_transformer_joint_causal_b300 import build as dit_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dit_attn.h")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    dit_build.build()
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(dit_attn_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_binding_symbols():
+    assert _declared() == sorted(dit.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(dit.library_path())
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings():
+    assert dit.version() >= 100
+    for code in range(7):
+        assert dit.status_string(code)
+    assert dit.status_string(99) == "unknown status"
+
+
+def _has_gpu():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+A = 0x7f0000000000   # fake, 16-byte aligned addresses: never dereferenced by a rejected call
+MB = 1 << 20
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((0, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 8, 8, 64, 0.125), 1),            # null q
+    ((A, A + MB, A + 2 * MB, 0, 1, 1, 8, 8, 64, 0.125), 1),                     # null out
+    ((A, A + MB, A + 2 * MB, A + 3 * MB, 0, 1, 8, 8, 64, 0.125), 1),            # B = 0
+    ((A, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 0, 8, 64, 0.125), 1),            # Lq = 0
+    ((A, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 8, 0, 64, 0.125), 1),            # Lk = 0
+    ((A, A + MB, A + 2 * MB, A + 3 * MB, 1, -2, 8, 8, 64, 0.125), 1),           # H < 0
+    ((A + 8, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 8, 8, 64, 0.125), 1),        # misaligned q
+    ((A, A + MB, A + 2 * MB, A + 3 * MB + 2, 1, 1, 8, 8, 64, 0.125), 1),        # misaligned out
+    ((A, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 8, 8, 64, float("nan")), 1),     # NaN scale
+    ((A, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 8, 8, 64, float("inf")), 1),     # inf scale
+    ((A, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 8, 8, 64, -0.5), 1),             # negative scale
+    ((A, A + MB, A + 2 * MB, A + 512, 1, 1, 8, 8, 64, 0.125), 1),               # out overlaps q
+    ((A, A + MB, A + 2 * MB, A + MB + 512, 1, 1, 8, 8, 64, 0.125), 1),          # out overlaps k
+    ((A, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 8, 8, 96, 0.125), 2),            # d = 96
+    ((A, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 8, 8, 256, 0.125), 2),           # d = 256
+    ((A, A + MB, A + 2 * MB, A + 3 * MB, 65536, 65536, 8, 8, 64, 0.125), 2),    # B*H too large
+    ((A, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 2**31 - 1, 8, 64, 0.125), 2),    # Lq too large
+])
+def test_forward_rejects_bad_arguments(args, expect):
+    assert dit.forward_ptr(*args) == expect
+
+
+@pytest.mark.skipif(_has_gpu(), reason="checks the no-device path")
+def test_no_device_paths():
+    assert dit.forward_ptr(A, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 8, 8, 64, 0.125) == 4
+    lib = ctypes.CDLL(dit.library_path())
+    assert lib.dit_attn_create() == 4
+    assert lib.dit_attn_destroy() == 4
+    assert lib.dit_attn_get_device_error(None) == 4
+    with pytest.raises(dit.DitAttnError):
+        dit.create()
+
+
+def test_python_forward_checks_tensors():
+    import torch
+    x = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        dit.forward(x, x, x)                               # CPU tensors
+    with pytest.raises(TypeError):
+        dit.forward(x.float(), x, x)
