@@ -173,52 +173,59 @@ __device__ void load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK, const 
 }
 
 // ----------------------------------------------------------------- MMA issuer
-// The 14-bit start-address field of a descriptor holds (address >> 4); the
-// shared window is below 256 KB, so adding (bytes >> 4) to the descriptor
-// advances the start address without touching other fields.
+// Descriptor low words carry (address >> 4) in their 14-bit start field; the
+// shared window is below 256 KB, so adding (bytes >> 4) to a low word advances
+// the start address without touching the other fields.
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_lo, uint32_t k_lo) {
   using T = Traits<D>;
   constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, 0, 0);
-  const uint64_t qd = smem_desc_sw128(q_smem, 16, 1024);
-  const uint64_t kd = smem_desc_sw128(k_smem, 16, 1024);
-#pragma unroll 1
+  constexpr uint32_t hi = desc_hi_sw128(1024);
+#pragma unroll
   for (int k = 0; k < D / 16; ++k) {
-    // K step k: 16 columns = 32 bytes into the 128-byte swizzle span, box k/4.
-    const uint64_t off = ((k / 4) * T::kBoxBytes + (k % 4) * 32) >> 4;
-    mma_ss(d_tmem, qd + off, kd + off, idesc, k > 0 ? 1u : 0u);
+    // K step k: 16 columns = 32 bytes into the 128-byte swizzle span of box k/4.
+    const uint32_t off = ((k / 4) * T::kBoxBytes + (k % 4) * 32) >> 4;
+    mma_ss_lo(d_tmem, q_lo + off, k_lo + off, hi, idesc, k > 0 ? 1u : 0u);
   }
 }
 
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_lo,
                                          bool accumulate) {
-  using T = Traits<D>;
   constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, 0, 1);
-  // V is [keys][d] with d contiguous: the B operand in MN-major form.  The
-  // second 64-column box is LBO away; 8-key row groups are SBO = 1024 apart.
-  const uint64_t vd = smem_desc_sw128(v_smem, T::kBoxBytes, 1024);
-#pragma unroll 1
+  constexpr uint32_t hi = desc_hi_sw128(1024);
+#pragma unroll
   for (int k = 0; k < kBN / 16; ++k) {
     // K step k: 16 keys = 16 rows of 128 bytes; P columns hold bf16 pairs.
-    mma_ts(d_tmem, p_tmem + k * 8, vd + ((k * 16 * 128) >> 4), idesc,
-           (accumulate || k > 0) ? 1u : 0u);
+    mma_ts_lo(d_tmem, p_tmem + k * 8, v_lo + ((k * 16 * 128) >> 4), hi, idesc,
+              (accumulate || k > 0) ? 1u : 0u);
   }
 }
 
+// Run by the whole MMA warp so that barrier waits and descriptor arithmetic
+// stay warp-uniform; lane 0 alone issues the MMAs and the commits that track them.
 template <int D>
 __device__ void mma_role(const Params& p, const Shared& sh, uint32_t tmem) {
   using T = Traits<D>;
+  const bool leader = (threadIdx.x & 31) == 0;
   uint32_t stage = 0, phase = 0;
   uint32_t g = 0;    // key-tile iterations so far (P hand-offs per query tile)
   uint32_t it = 0;   // work units so far
   bool ok = true;
   const int n_kv = (p.Lk + kBN - 1) / kBN;
-  const uint32_t q_smem[2] = {sh.base + T::kOffQ, sh.base + T::kOffQ + T::kTileBytes};
-  auto kv_smem = [&](uint32_t s) { return sh.base + T::kOffKV + s * T::kTileBytes; };
+  // K-major Q/K tiles: LBO unused (16); V tiles (MN-major): LBO = one 64-column box.
+  const uint32_t q_lo0 = desc_lo_sw128(sh.base + T::kOffQ, 16);
+  const uint32_t q_lo1 = desc_lo_sw128(sh.base + T::kOffQ + T::kTileBytes, 16);
+  const uint32_t kv_lo0 = desc_lo_sw128(sh.base + T::kOffKV, 16);
+  const uint32_t v_lbo = ((T::kBoxBytes >> 4) << 16) - (1u << 16);   // LBO 16 -> one box
+  auto k_lo = [&](uint32_t s) { return kv_lo0 + s * (T::kTileBytes >> 4); };
+  auto wait = [&](int bar, uint32_t parity) -> bool {
+    const bool got = mbar_wait(sh.bar(bar), parity, kWaitLimitNs, sh.abort);
+    return __all_sync(0xffffffffu, got);
+  };
   auto take_stage = [&](uint32_t& s_out) -> bool {
     s_out = stage;
-    if (!mbar_wait(sh.bar(T::kBarFull + stage), phase, kWaitLimitNs, sh.abort)) return false;
+    if (!wait(T::kBarFull + stage, phase)) return false;
     if (++stage == T::kStages) { stage = 0; phase ^= 1u; }
     return true;
   };
@@ -226,56 +233,69 @@ __device__ void mma_role(const Params& p, const Shared& sh, uint32_t tmem) {
   for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++it) {
     uint32_t sK = 0, sV = 0;
     // S_t = Q_t K_0^T for both tiles
-    ok = mbar_wait(sh.bar(T::kBarQFull + 0), it & 1u, kWaitLimitNs, sh.abort) && take_stage(sK);
+    ok = wait(T::kBarQFull + 0, it & 1u) && take_stage(sK);
     if (!ok) break;
     tc_fence_after();
-    issue_qk<D>(tmem + T::col_s(0), q_smem[0], kv_smem(sK));
-    mma_commit(sh.bar(T::kBarSFull + 0));
-    if (n_kv == 1) mma_commit(sh.bar(T::kBarQEmpty + 0));
-    ok = mbar_wait(sh.bar(T::kBarQFull + 1), it & 1u, kWaitLimitNs, sh.abort);
+    if (leader) {
+      issue_qk<D>(tmem + T::col_s(0), q_lo0, k_lo(sK));
+      mma_commit(sh.bar(T::kBarSFull + 0));
+      if (n_kv == 1) mma_commit(sh.bar(T::kBarQEmpty + 0));
+    }
+    __syncwarp();
+    ok = wait(T::kBarQFull + 1, it & 1u);
     if (!ok) break;
     tc_fence_after();
-    issue_qk<D>(tmem + T::col_s(1), q_smem[1], kv_smem(sK));
-    mma_commit(sh.bar(T::kBarSFull + 1));
-    if (n_kv == 1) mma_commit(sh.bar(T::kBarQEmpty + 1));
-    mma_commit(sh.bar(T::kBarEmpty + sK));
+    if (leader) {
+      issue_qk<D>(tmem + T::col_s(1), q_lo1, k_lo(sK));
+      mma_commit(sh.bar(T::kBarSFull + 1));
+      if (n_kv == 1) mma_commit(sh.bar(T::kBarQEmpty + 1));
+      mma_commit(sh.bar(T::kBarEmpty + sK));
+    }
+    __syncwarp();
 
     for (int j = 0; j < n_kv && ok; ++j, ++g) {
       const bool more = j + 1 < n_kv;
-      ok = take_stage(sV) && mbar_wait(sh.bar(T::kBarPFull + 0), g & 1u, kWaitLimitNs, sh.abort);
+      ok = take_stage(sV) && wait(T::kBarPFull + 0, g & 1u);
+      if (more) ok = ok && take_stage(sK);
       if (!ok) break;
       tc_fence_after();
-      issue_pv<D>(tmem + T::col_o(0), tmem + T::col_s(0), kv_smem(sV), j > 0);
-      if (more) {
-        ok = take_stage(sK);
-        if (!ok) break;
-        tc_fence_after();
-        issue_qk<D>(tmem + T::col_s(0), q_smem[0], kv_smem(sK));
-        mma_commit(sh.bar(T::kBarSFull + 0));
-        if (j + 2 == n_kv) mma_commit(sh.bar(T::kBarQEmpty + 0));
-      } else {
-        mma_commit(sh.bar(T::kBarOFull + 0));
+      if (leader) {
+        issue_pv<D>(tmem + T::col_o(0), tmem + T::col_s(0), k_lo(sV) + v_lbo, j > 0);
+        if (more) {
+          issue_qk<D>(tmem + T::col_s(0), q_lo0, k_lo(sK));
+          mma_commit(sh.bar(T::kBarSFull + 0));
+          if (j + 2 == n_kv) mma_commit(sh.bar(T::kBarQEmpty + 0));
+        } else {
+          mma_commit(sh.bar(T::kBarOFull + 0));
+        }
       }
-      ok = mbar_wait(sh.bar(T::kBarPFull + 1), g & 1u, kWaitLimitNs, sh.abort);
+      __syncwarp();
+      ok = wait(T::kBarPFull + 1, g & 1u);
       if (!ok) break;
       tc_fence_after();
-      issue_pv<D>(tmem + T::col_o(1), tmem + T::col_s(1), kv_smem(sV), j > 0);
-      mma_commit(sh.bar(T::kBarEmpty + sV));
-      if (more) {
-        issue_qk<D>(tmem + T::col_s(1), q_smem[1], kv_smem(sK));
-        mma_commit(sh.bar(T::kBarSFull + 1));
-        if (j + 2 == n_kv) mma_commit(sh.bar(T::kBarQEmpty + 1));
-        mma_commit(sh.bar(T::kBarEmpty + sK));
-      } else {
-        mma_commit(sh.bar(T::kBarOFull + 1));
+      if (leader) {
+        issue_pv<D>(tmem + T::col_o(1), tmem + T::col_s(1), k_lo(sV) + v_lbo, j > 0);
+        mma_commit(sh.bar(T::kBarEmpty + sV));
+        if (more) {
+          issue_qk<D>(tmem + T::col_s(1), q_lo1, k_lo(sK));
+          mma_commit(sh.bar(T::kBarSFull + 1));
+          if (j + 2 == n_kv) mma_commit(sh.bar(T::kBarQEmpty + 1));
+          mma_commit(sh.bar(T::kBarEmpty + sK));
+        } else {
+          mma_commit(sh.bar(T::kBarOFull + 1));
+        }
       }
+      __syncwarp();
     }
   }
-  if (!ok) record_timeout(sh);
-  // Drain: every MMA this thread issued completes before TMEM is released.
-  mma_commit(sh.bar(T::kBarDrain));
-  const volatile int no_abort = 0;
-  mbar_wait(sh.bar(T::kBarDrain), 0, kWaitLimitNs, &no_abort);
+  if (!ok && leader) record_timeout(sh);
+  // Drain: every MMA lane 0 issued completes before TMEM is released.
+  if (leader) {
+    mma_commit(sh.bar(T::kBarDrain));
+    const volatile int no_abort = 0;
+    mbar_wait(sh.bar(T::kBarDrain), 0, kWaitLimitNs, &no_abort);
+  }
+  __syncwarp();
 }
 
 // ----------------------------------------------------------------- softmax + epilogue
@@ -479,8 +499,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     softmax_role<D>(p, sh, tmem, warp / 4);
   } else if (warp == kMmaWarp) {
     reg_dealloc<kRegsOther>();
-    if (lane == 0) mma_role<D>(p, sh, tmem);
-    __syncwarp();
+    mma_role<D>(p, sh, tmem);
   } else if (warp == kLoadWarp) {
     reg_dealloc<kRegsOther>();
     if (lane == 0) load_role<D>(&tmQ, &tmK, &tmV, p, sh);
