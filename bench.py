@@ -95,8 +95,47 @@ def recorded_traffic(workload: str):
     return None
 
 
+class _Nvml:
+    """Read-only NVML queries through ctypes (SM clock, max clock, clock-event reasons)."""
+
+    def __init__(self, bus_id: str | None, index: int):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        rc = 1
+        if bus_id:
+            rc = self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus_id.encode(), ctypes.byref(self.h))
+        if rc != 0:
+            rc = self.lib.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.h))
+        if rc != 0:
+            raise RuntimeError("no NVML handle")
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self.reasons_fn = fn or self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def _clock(self, fn):
+        v = self.c.c_uint()
+        if fn(self.h, 1, self.c.byref(v)) != 0:   # NVML_CLOCK_SM
+            raise RuntimeError("clock query failed")
+        return int(v.value)
+
+    def sm_mhz(self):
+        return self._clock(self.lib.nvmlDeviceGetClockInfo)
+
+    def max_sm_mhz(self):
+        return self._clock(self.lib.nvmlDeviceGetMaxClockInfo)
+
+    def reasons(self):
+        v = self.c.c_ulonglong()
+        if self.reasons_fn(self.h, self.c.byref(v)) != 0:
+            raise RuntimeError("reason query failed")
+        return int(v.value)
+
+
 class ClockSampler:
-    """Polls SM clock, power and clock-event reasons through NVML while running."""
+    """Samples SM clock and clock-event reasons while the timed region runs."""
 
     REASONS = {  # NVML clocks-event reason bits
         0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
@@ -105,42 +144,49 @@ class ClockSampler:
         0x100: "display_clock_setting",
     }
 
-    def __init__(self, device_index: int, period_s: float = 0.01):
+    def __init__(self, device_index: int, bus_id: str | None = None, period_s: float = 0.01):
         self.samples = []
         self.period = period_s
-        self.ok = False
         self.max_mhz = None
-        try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception:
-            self.ok = False
+        self.source = None
         self._stop = threading.Event()
         self._t = None
-
-    def _reasons(self):
         try:
-            return self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+            self.nv = _Nvml(bus_id, device_index)
+            self.max_mhz = self.nv.max_sm_mhz()
+            self.source = "nvml"
         except Exception:
-            return self.nv.nvmlDeviceGetCurrentClocksThrottleReasons(self.h)
+            self.nv = None
+            self.source = "nvidia-smi"
+        self.index = device_index
+        self.bus_id = bus_id
 
-    def _run(self):
+    def _run_nvml(self):
         while not self._stop.is_set():
             try:
-                self.samples.append((self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM),
-                                     self._reasons()))
+                self.samples.append((self.nv.sm_mhz(), self.nv.reasons()))
             except Exception:
                 pass
             time.sleep(self.period)
 
+    def _run_smi(self):
+        import subprocess
+        target = self.bus_id or str(self.index)
+        q = "clocks.sm,clocks.max.sm,clocks_event_reasons.active"
+        while not self._stop.is_set():
+            try:
+                out = subprocess.run(["nvidia-smi", "-i", target, f"--query-gpu={q}",
+                                      "--format=csv,noheader,nounits"], capture_output=True,
+                                     text=True, timeout=5).stdout.strip().split(",")
+                self.max_mhz = int(out[1])
+                self.samples.append((int(out[0]), int(out[2].strip(), 16)))
+            except Exception:
+                pass
+            time.sleep(max(self.period, 0.05))
+
     def start(self):
-        if self.ok:
-            self._t = threading.Thread(target=self._run, daemon=True)
-            self._t.start()
+        self._t = threading.Thread(target=self._run_nvml if self.nv else self._run_smi, daemon=True)
+        self._t.start()
 
     def stop(self):
         if self._t:
@@ -148,16 +194,25 @@ class ClockSampler:
             self._t.join()
 
     def summary(self):
-        if not self.ok or not self.samples:
+        if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"],
-                    "samples": 0}
+                    "samples": 0, "source": self.source}
         mhz = [s[0] for s in self.samples]
         bits = 0
         for _, r in self.samples:
             bits |= int(r)
         reasons = [name for bit, name in self.REASONS.items() if bits & bit and name != "gpu_idle"]
         return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz,
-                "reasons": reasons, "samples": len(mhz)}
+                "reasons": reasons, "samples": len(mhz), "source": self.source}
+
+
+def pci_bus_id(dev_index: int):
+    try:
+        import torch
+        pr = torch.cuda.get_device_properties(dev_index)
+        return f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+    except Exception:
+        return None
 
 
 def dist_env():
@@ -165,6 +220,31 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def reduce_max_fn(world: int, device=None):
+    """max over ranks of a float (identity on one rank); gloo or nccl process group."""
+    if world == 1:
+        return lambda x: x
+
+    def reduce(x: float) -> float:
+        import torch
+        import torch.distributed as tdist
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        return float(t.item())
+    return reduce
+
+
+def replica_throughput(local_ms: float, flops_per_step: float, steps: int, world: int,
+                       reduce_max) -> tuple:
+    """Whole-job TFLOP/s of `world` replicas that each ran `steps` steps.
+
+    The job's time is the slowest rank's (max over ranks); the work is every
+    rank's steps.  Returns (TFLOP/s, max ms).
+    """
+    max_ms = reduce_max(local_ms)
+    return world * flops_per_step * steps / (max_ms / 1e3) / 1e12, max_ms
 
 
 def oracle_sample(w, n_rows, n_threads):
@@ -267,13 +347,7 @@ def bench_ours(args):
             import torch.distributed as tdist
             tdist.barrier()
 
-    def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        import torch.distributed as tdist
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-        return float(t.item())
+    max_over_ranks = reduce_max_fn(world, dev)
 
     qb, kb, vb = W.make_qkv(w)
     host = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in (qb, kb, vb)]
@@ -287,7 +361,7 @@ def bench_ours(args):
     for _ in range(max(args.warmup, 3)):
         dit.forward(q, k, v, w.scale, out=out)
     torch.cuda.synchronize(dev)
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(local, pci_bus_id(local))
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     barrier()
     torch.cuda.synchronize(dev)
@@ -301,8 +375,7 @@ def bench_ours(args):
     barrier()
     per_launch = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
     total_ms = ev[0].elapsed_time(ev[args.steps])
-    max_ms = max_over_ranks(total_ms)
-    value = world * flops * args.steps / (max_ms / 1e3) / 1e12
+    value, max_ms = replica_throughput(total_ms, flops, args.steps, world, max_over_ranks)
     if dit.get_device_error() != 0:
         raise RuntimeError("device-side wait timed out during the benchmark")
 
@@ -327,8 +400,8 @@ def bench_ours(args):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1))
-    e2e_value = world * flops * args.e2e_steps / (e2e_ms / 1e3) / 1e12
+    e2e_value, _ = replica_throughput(e0.elapsed_time(e1), flops, args.e2e_steps, world,
+                                      max_over_ranks)
 
     if rank != 0:
         if world > 1:

@@ -18,6 +18,7 @@ import os
 import threading
 
 __all__ = ["create", "destroy", "forward", "forward_ptr", "status_string", "get_device_error",
+           "check_wait_timeout",
            "last_cuda_error", "version", "library_path", "DitAttnError", "STATUS",
            "EXPORTED_SYMBOLS"]
 
@@ -31,7 +32,7 @@ STATUS = {
 
 EXPORTED_SYMBOLS = ("dit_attn_version", "dit_attn_create", "dit_attn_forward",
                     "dit_attn_destroy", "dit_attn_status_string", "dit_attn_get_device_error",
-                    "dit_attn_last_cuda_error")
+                    "dit_attn_check_wait_timeout", "dit_attn_last_cuda_error")
 
 _lock = threading.Lock()
 _lib = None
@@ -72,6 +73,8 @@ def _load():
             lib.dit_attn_status_string.argtypes = [c_int]
             lib.dit_attn_get_device_error.restype = c_int
             lib.dit_attn_get_device_error.argtypes = [vp]
+            lib.dit_attn_check_wait_timeout.restype = c_int
+            lib.dit_attn_check_wait_timeout.argtypes = [c_int, vp]
             lib.dit_attn_last_cuda_error.restype = c_int
             lib.dit_attn_last_cuda_error.argtypes = []
             _lib = lib
@@ -113,6 +116,11 @@ def _stream_handle(stream):
 def get_device_error(stream=None) -> int:
     """Synchronise the stream and return (and clear) the kernels' error word."""
     return _load().dit_attn_get_device_error(_stream_handle(stream))
+
+
+def check_wait_timeout(limit_us: int, stream=None) -> int:
+    """Enqueue the bounded-wait self-test kernel; returns the launch status."""
+    return _load().dit_attn_check_wait_timeout(int(limit_us), _stream_handle(stream))
 
 
 def forward_ptr(q: int, k: int, v: int, out: int, B: int, H: int, Lq: int, Lk: int, d: int,

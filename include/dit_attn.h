@@ -3,11 +3,12 @@
  * joint text+image token sequence of a diffusion transformer, on NVIDIA B300
  * (sm_103a).
  *
- * The operation is standard attention, the "traditional / standard BF16
- * attention" that "Speed Up Image Generation with FLUX 3 Image Klein on NVIDIA
- * Blackwell GPUs" (attention paragraph; also the Japanese summary on
- * sns.style, fourth paragraph) measures at about 60% of DiT kernel time at
- * 2048x2048.  For every batch b, head h and query row i:
+ * The operation is standard attention, the dense BF16 attention that "Speed Up
+ * Image Generation with FLUX 3 Image Klein on NVIDIA Blackwell GPUs" (Key
+ * takeaways, second item) and the diegocecato.dcsolution.it article
+ * "flux-3-blackwell-denoising-latenza-pipeline" (section "NVFP4, attention e
+ * caching") put at about 60% of DiT kernel time at 2048x2048.  For every
+ * batch b, head h and query row i:
  *
  *     s_ij = scale * sum_c q[b,h,i,c] * k[b,h,j,c]        (j < Lk, no mask)
  *     o[b,h,i,:] = sum_j softmax_j(s_ij) * v[b,h,j,:]
@@ -63,7 +64,8 @@ int dit_attn_create(void);
 
 /*
  * out = softmax(q k^T * scale) v for every (batch, head), enqueued on stream.
- *   B, H, Lq, Lk >= 1; B*H*max(Lq,Lk)*d < 2^31; Lq, Lk < 2^31.
+ *   B, H, Lq, Lk >= 1; B*H < 2^31; Lq, Lk <= 2^31 - 513;
+ *   B*H*ceil(Lq/256) < 2^31 (else UNSUPPORTED).
  *   d in {64, 128}.
  *   scale finite and >= 0 (1/sqrt(d) for a standard transformer).
  * Asynchronous: returns after the launch.  A launch failure returns
@@ -85,6 +87,16 @@ const char* dit_attn_status_string(int status);
  * if the synchronisation itself failed).  A test and debugging aid.
  */
 int dit_attn_get_device_error(void* stream);
+
+/*
+ * Self-test of failure detection: enqueue a one-thread kernel that waits on a
+ * barrier nothing ever completes, gives up after limit_us microseconds
+ * (1 .. 1000000, else INVALID_ARG) and sets the device error word exactly as
+ * an attention kernel does when a bounded wait gives up.  A following
+ * dit_attn_get_device_error then returns TIMEOUT, and the context stays
+ * usable.  Nothing faults or hangs.  Requires dit_attn_create().
+ */
+int dit_attn_check_wait_timeout(int limit_us, void* stream);
 
 /* The cudaError_t behind the most recent DIT_ATTN_ERR_CUDA on this thread. */
 int dit_attn_last_cuda_error(void);

@@ -8,9 +8,9 @@ product: the two share only the seeded input generator in ``workloads``.
 The arithmetic lives in ``attn_oracle.c`` (plain C, double precision, libm
 ``exp``, no fast-math); this module compiles it with gcc on first use and
 marshals numpy arrays through ctypes.  What it computes is the textbook
-definition of standard attention (the "traditional BF16 attention" baseline of
-"Speed Up Image Generation with FLUX 3 Image Klein on NVIDIA Blackwell GPUs",
-attention paragraph): o_i = sum_j softmax_j(scale * q_i . k_j) v_j.
+definition of standard attention (the dense BF16 attention that "Speed Up
+Image Generation with FLUX 3 Image Klein on NVIDIA Blackwell GPUs", Key
+takeaways, second item, measures): o_i = sum_j softmax_j(scale * q_i . k_j) v_j.
 
 Pins (tests/test_oracle_pins.py) tie it to things other than itself: a
 50-digit decimal brute force on tiny inputs, the two-key sigmoid closed form,

@@ -5,10 +5,10 @@
  * benchmark's CPU-baseline leg load this file's library.  It shares no code,
  * header, table or helper with the CUDA path.
  *
- * What it computes (the definition of standard attention, the baseline the
- * pages call "traditional / standard BF16 attention" in "Speed Up Image
- * Generation with FLUX 3 Image Klein on NVIDIA Blackwell GPUs", attention
- * paragraph): for one query row i of head (b,h)
+ * What it computes (the definition of standard attention: the dense BF16
+ * attention that "Speed Up Image Generation with FLUX 3 Image Klein on NVIDIA
+ * Blackwell GPUs", Key takeaways, second item, measures at about 60% of DiT
+ * kernel time): for one query row i of head (b,h)
  *
  *     s_j = scale * sum_c q[i,c] * k[j,c]            j = 0 .. Lk-1
  *     m   = max_j s_j

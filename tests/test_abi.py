@@ -97,3 +97,9 @@ def test_python_forward_checks_tensors():
         dit.forward(x, x, x)                               # CPU tensors
     with pytest.raises(TypeError):
         dit.forward(x.float(), x, x)
+
+
+def test_wait_timeout_check_validates_before_cuda():
+    lib = ctypes.CDLL(dit.library_path())
+    assert lib.dit_attn_check_wait_timeout(0, None) == 1
+    assert lib.dit_attn_check_wait_timeout(2000000, None) == 1

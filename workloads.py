@@ -5,11 +5,12 @@ oracle's tests.  It holds no attention arithmetic: it only draws random
 numbers, applies the per-token RMS normalisation that some workloads ask for,
 and rounds float32 to bfloat16 bit patterns.
 
-Workloads (shapes follow the FLUX-3-Image-Klein-class DiT the pages describe:
-"Speed Up Image Generation with FLUX 3 Image Klein on NVIDIA Blackwell GPUs",
-the latency-breakdown and attention paragraphs, which put dense BF16 attention
-at about 60% of DiT kernel time at 2048x2048).  The head count, head dim and
-token counts are not printed on the pages; they are the stated workload sizes:
+Workloads (shapes follow the FLUX-3-Image-Klein-class DiT of "Speed Up Image
+Generation with FLUX 3 Image Klein on NVIDIA Blackwell GPUs", Key takeaways,
+second item: denoising dominates at 2048x2048 and dense BF16 attention takes
+about 60% of DiT kernel time; 1024x1024 and 2048x2048 text-to-image and
+image-to-image are the pages' workloads).  The head count, head dim and token
+counts are not printed on the pages; they are the stated workload sizes:
 
   tiny            B=1 H=2  L=256   (64 text + 192 image)           d=64   N(0,1)
   1024px          B=1 H=24 L=4608  (4096 image + 512 text)         d=128  N(0,1), Q/K RMS-normed
