@@ -58,6 +58,7 @@ constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s per wait
 constexpr float kRescaleThreshold = 8.0f;          // log2 units
+constexpr float kOptimisticSumLimit = 65536.0f;    // 2^16: a tile sum above it forces the max
 
 template <int D>
 struct Traits {
@@ -104,8 +105,15 @@ struct Shared {
   __device__ uint32_t bar(int i) const { return bar0 + 8u * static_cast<uint32_t>(i); }
 };
 
+// Give up: stop every role of this CTA (and, for a CTA pair, of the peer CTA)
+// and record TIMEOUT in the device error word.
+template <bool kPair = false>
 __device__ __forceinline__ void record_timeout(const Shared& sh) {
   *sh.abort = 1;
+  if (kPair) {
+    const uint32_t local = smem_u32(const_cast<int*>(sh.abort));
+    st_shared_cluster_u32(mapa_shared(local, cluster_ctarank() ^ 1u), 1u);
+  }
   atomicExch(&g_device_error, DIT_ATTN_ERR_TIMEOUT);
 }
 
@@ -314,53 +322,44 @@ __device__ __forceinline__ void rescale_o(uint32_t taddr_o, float factor) {
   }
 }
 
-// exp2 of one S tile into packed bf16 probabilities, written back over the
-// first 64 TMEM columns of S (each half as soon as it is packed).  Returns the
-// sum of the probabilities *as rounded to bf16*, so that the row sum l and the
-// P.V product weigh every key identically (a row dominated by one key then
-// returns that key's value row without a rounding-induced scale error).
-// kMasked: keys at or beyond `valid` get probability 0.
+// exp2 of one S tile into packed bf16 probabilities (pk[i] holds keys 2i and
+// 2i+1).  Returns the sum of the probabilities *as rounded to bf16*, so that
+// the row sum l and the P.V product weigh every key identically (a row
+// dominated by one key then returns that key's value row without a
+// rounding-induced scale error); the sum uses mixed-precision f32 += bf16 adds
+// on the packed halves.  kMasked: keys at or beyond `valid` get probability 0.
 template <bool kMasked>
 __device__ __forceinline__ float probs_tile(const uint32_t (&sr)[4][32], float scale_log2,
-                                            float neg_m, int valid, uint32_t taddr_p) {
+                                            float neg_m, int valid, uint32_t (&pk)[64]) {
   const float2 sl2 = make_float2(scale_log2, scale_log2);
   const float2 nm = make_float2(neg_m, neg_m);
-  float2 acc[4];
+  float acc[8];
 #pragma unroll
-  for (int a = 0; a < 4; ++a) acc[a] = make_float2(0.f, 0.f);
+  for (int a = 0; a < 8; ++a) acc[a] = 0.f;
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    uint32_t pk[32];
+  for (int c = 0; c < 4; ++c)
 #pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
-      const int c = 2 * h + cc;
-#pragma unroll
-      for (int i = 0; i < 32; i += 2) {
-        const float2 x = __ffma2_rn(
-            make_float2(__uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1])), sl2, nm);
-        float p0 = ex2_approx(x.x);
-        float p1 = ex2_approx(x.y);
-        if (kMasked) {
-          p0 = (c * 32 + i < valid) ? p0 : 0.f;
-          p1 = (c * 32 + i + 1 < valid) ? p1 : 0.f;
-        }
-        const uint32_t w = pack_bf16x2(p0, p1);
-        pk[cc * 16 + i / 2] = w;
-        acc[(i / 2) & 3] = __fadd2_rn(
-            acc[(i / 2) & 3], make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)));
+    for (int i = 0; i < 32; i += 2) {
+      const float2 x = __ffma2_rn(
+          make_float2(__uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1])), sl2, nm);
+      float p0 = ex2_approx(x.x);
+      float p1 = ex2_approx(x.y);
+      if (kMasked) {
+        p0 = (c * 32 + i < valid) ? p0 : 0.f;
+        p1 = (c * 32 + i + 1 < valid) ? p1 : 0.f;
       }
+      const uint32_t w = pack_bf16x2(p0, p1);
+      pk[c * 16 + i / 2] = w;
+      add_bf16x2_halves(acc[(i / 2) & 7], acc[((i / 2) + 4) & 7], w);
     }
-    tmem_st32(taddr_p + h * 32, pk);
-  }
-  const float2 s01 = __fadd2_rn(acc[0], acc[1]);
-  const float2 s23 = __fadd2_rn(acc[2], acc[3]);
-  const float2 s = __fadd2_rn(s01, s23);
-  return s.x + s.y;
+  return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
 }
 
 template <bool kMasked>
 __device__ __forceinline__ float rowmax_tile(const uint32_t (&sr)[4][32], int valid) {
-  float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  float m[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) m[k] = -INFINITY;
 #pragma unroll
   for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -370,14 +369,16 @@ __device__ __forceinline__ float rowmax_tile(const uint32_t (&sr)[4][32], int va
         a = (c * 32 + i < valid) ? a : -INFINITY;
         b = (c * 32 + i + 1 < valid) ? b : -INFINITY;
       }
-      m[(i / 2) & 3] = fmax3(m[(i / 2) & 3], a, b);
+      m[(c * 16 + i / 2) & 7] = fmax3(m[(c * 16 + i / 2) & 7], a, b);
     }
-  return fmax3(m[0], m[1], fmaxf(m[2], m[3]));
+  return fmaxf(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], fmax3(m[5], m[6], m[7])));
 }
 
-template <int D>
+// kPair: the CTA is one half of a pair; a work unit then spans 512 query rows
+// (this CTA's 256 start at rank*256) and P-ready is reported, one arrival per
+// warp, on the barrier of the pair's leader CTA, whose warp issues the MMAs.
+template <int D, class T, bool kPair>
 __device__ void softmax_role(const Params& p, const Shared& sh, uint32_t tmem, int t) {
-  using T = Traits<D>;
   const int wg_warp = (threadIdx.x / 32) & 3;
   const int r = wg_warp * 32 + (threadIdx.x & 31);   // row within the query tile
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(wg_warp * 32) << 16);
@@ -388,10 +389,15 @@ __device__ void softmax_role(const Params& p, const Shared& sh, uint32_t tmem, i
   const int tail = p.Lk - (n_kv - 1) * kBN;   // valid keys in the last tile, 1..128
   uint32_t g = 0, it = 0;
   bool ok = true;
+  const int rank = kPair ? static_cast<int>(cluster_ctarank()) : 0;
+  const int u0 = kPair ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int u_stride = kPair ? static_cast<int>(num_clusters_x()) : static_cast<int>(gridDim.x);
+  const int unit_rows = kPair ? 2 * kUnitRows : kUnitRows;
+  const uint32_t p_full_leader = kPair ? mapa_shared(sh.bar(T::kBarPFull + t), 0) : 0u;
 
-  for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++it) {
+  for (int u = u0; u < p.num_units && ok; u += u_stride, ++it) {
     const int bh = u / p.num_qblocks;
-    const int row = (u % p.num_qblocks) * kUnitRows + t * kBM + r;
+    const int row = (u % p.num_qblocks) * unit_rows + rank * kUnitRows + t * kBM + r;
     float m_used = -INFINITY;   // running max, in units of s*scale*log2(e)
     float l = 0.f;
     for (int j = 0; j < n_kv; ++j, ++g) {
@@ -403,22 +409,52 @@ __device__ void softmax_role(const Params& p, const Shared& sh, uint32_t tmem, i
       for (int c = 0; c < 4; ++c) tmem_ld32(taddr_s + c * 32, sr[c]);
       tmem_wait_ld();
       const bool masked = (j == n_kv - 1) && (tail < kBN);
-      const float mx = masked ? rowmax_tile<true>(sr, tail) : rowmax_tile<false>(sr, kBN);
-      const float m_tile = mx * scale_log2;
-      float factor = 1.f;
-      if (m_tile > m_used + kRescaleThreshold) {
-        factor = ex2_approx(m_used - m_tile);   // 0 on the first tile
-        l *= factor;
-        m_used = m_tile;
+      const int valid = masked ? tail : kBN;
+      uint32_t pk[64];
+      float tile_sum;
+      // Row max, lazy rescale of l and O, probabilities (first tile, or a redo).
+      auto max_pass = [&]() {
+        const float mx = masked ? rowmax_tile<true>(sr, tail) : rowmax_tile<false>(sr, kBN);
+        const float m_tile = mx * scale_log2;
+        float factor = 1.f;
+        if (m_tile > m_used + kRescaleThreshold) {
+          factor = ex2_approx(m_used - m_tile);   // 0 on the first tile
+          l *= factor;
+          m_used = m_tile;
+        }
+        // O_t is quiescent here: S_t's completion implies the previous P.V product finished.
+        if (j > 0 && __any_sync(0xffffffffu, factor != 1.f)) rescale_o<D>(taddr_o, factor);
+        return masked ? probs_tile<true>(sr, scale_log2, -m_used, valid, pk)
+                      : probs_tile<false>(sr, scale_log2, -m_used, kBN, pk);
+      };
+      if (j == 0) {
+        tile_sum = max_pass();
+      } else {
+        // Optimistic pass against the running max.  A tile whose rounded sum
+        // exceeds 2^16 has some p > 2^9: it reloads S (still intact in TMEM,
+        // P is not stored yet), raises the max (always, since p > 2^8),
+        // rescales l and O and recomputes.  Warp-uniform branch: the TMEM
+        // accesses stay collective.
+        tile_sum = masked ? probs_tile<true>(sr, scale_log2, -m_used, valid, pk)
+                          : probs_tile<false>(sr, scale_log2, -m_used, kBN, pk);
+        if (__any_sync(0xffffffffu, !(tile_sum <= kOptimisticSumLimit))) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld32(taddr_s + c * 32, sr[c]);
+          tmem_wait_ld();
+          tile_sum = max_pass();
+        }
       }
-      // O_t is quiescent here: S_t's completion implies the previous P.V product finished.
-      if (j > 0 && __any_sync(0xffffffffu, factor != 1.f)) rescale_o<D>(taddr_o, factor);
-      const float neg_m = -m_used;
-      l += masked ? probs_tile<true>(sr, scale_log2, neg_m, tail, taddr_s)
-                  : probs_tile<false>(sr, scale_log2, neg_m, kBN, taddr_s);
+      l += tile_sum;
+      tmem_st32(taddr_s, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+      tmem_st32(taddr_s + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(sh.bar(T::kBarPFull + t));
+      if (kPair) {
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive_cluster(p_full_leader);
+      } else {
+        mbar_arrive(sh.bar(T::kBarPFull + t));
+      }
     }
     if (!ok) break;
     // Epilogue: O_t / l -> bf16 -> global, one contiguous row per thread.
@@ -444,7 +480,7 @@ __device__ void softmax_role(const Params& p, const Shared& sh, uint32_t tmem, i
       }
     }
   }
-  if (!ok) record_timeout(sh);
+  if (!ok) record_timeout<kPair>(sh);
 }
 
 // ----------------------------------------------------------------- kernel
@@ -497,7 +533,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
   if (warp < kMmaWarp) {
     reg_alloc<kRegsSoftmax>();
-    softmax_role<D>(p, sh, tmem, warp / 4);
+    softmax_role<D, Traits<D>, false>(p, sh, tmem, warp / 4);
   } else if (warp == kMmaWarp) {
     reg_dealloc<kRegsOther>();
     mma_role<D>(p, sh, tmem);
@@ -535,6 +571,8 @@ __global__ void wait_timeout_kernel(uint64_t limit_ns) {
 
 }  // namespace dit
 
+#include "fmha_pair.cuh"
+
 // =================================================================== host side
 namespace {
 
@@ -543,6 +581,7 @@ using dit::Traits;
 struct DeviceState {
   bool ready = false;
   int num_sms = 0;
+  int max_pairs = 0;   // co-resident clusters of two CTAs of the pair kernel
 };
 
 constexpr int kMaxDevices = 64;
@@ -564,14 +603,16 @@ bool current_device(int* dev) {
   return *dev >= 0 && *dev < kMaxDevices;
 }
 
-// 3-D bf16 view [BH][L][d] with a 64-column x 128-row box and 128-byte swizzle.
-// Rows beyond L inside one head read as zeros, never as the next head's rows.
-int encode_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t L, int d) {
+// 3-D bf16 view [BH][L][d] with a 64-column x box_rows box and 128-byte
+// swizzle.  Rows beyond L inside one head read as zeros, never as the next
+// head's rows.
+int encode_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t L, int d,
+               uint32_t box_rows = 128) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(L),
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                                  static_cast<cuuint64_t>(L) * static_cast<cuuint64_t>(d) * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t box[3] = {64, box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -607,6 +648,44 @@ int launch(const void* q, const void* k, const void* v, void* out, int64_t BH, i
   const int grid = p.num_units < num_sms ? p.num_units : num_sms;
   dit::fmha_fwd_kernel<D><<<grid, dit::kNumThreads, Traits<D>::kSmemBytes, stream>>>(tq, tk, tv, p);
   const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return DIT_ATTN_OK;
+}
+
+cudaLaunchConfig_t pair_launch_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(dit::kNumThreads, 1, 1);
+  cfg.dynamicSmemBytes = dit::PairTraits::kSmemBytes;
+  cfg.stream = stream;
+  attr->id = cudaLaunchAttributeClusterDimension;
+  attr->val.clusterDim.x = 2;
+  attr->val.clusterDim.y = 1;
+  attr->val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+// d = 128: clusters of two CTAs, one work unit = 512 query rows.
+int launch_pair(const void* q, const void* k, const void* v, void* out, int64_t BH, int Lq, int Lk,
+                float scale, cudaStream_t stream, int max_pairs) {
+  CUtensorMap tq, tk, tv;
+  int rc;
+  if ((rc = encode_map(&tq, q, BH, Lq, 128, 128)) != DIT_ATTN_OK) return rc;
+  if ((rc = encode_map(&tk, k, BH, Lk, 128, 64)) != DIT_ATTN_OK) return rc;
+  if ((rc = encode_map(&tv, v, BH, Lk, 128, 128)) != DIT_ATTN_OK) return rc;
+  dit::Params p;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.num_qblocks = (Lq + 2 * dit::kUnitRows - 1) / (2 * dit::kUnitRows);
+  p.num_units = static_cast<int>(BH * p.num_qblocks);
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  const int pairs = p.num_units < max_pairs ? p.num_units : max_pairs;
+  cudaLaunchAttribute attr;
+  cudaLaunchConfig_t cfg = pair_launch_config(2 * pairs, stream, &attr);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, dit::fmha_fwd_pair_kernel, tq, tk, tv, p);
   if (e != cudaSuccess) return cuda_fail(e);
   return DIT_ATTN_OK;
 }
@@ -655,6 +734,20 @@ int dit_attn_create(void) {
   e = cudaFuncSetAttribute(dit::fmha_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Traits<128>::kSmemBytes);
   if (e != cudaSuccess) return cuda_fail(e);
+  e = cudaFuncSetAttribute(dit::fmha_fwd_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           dit::PairTraits::kSmemBytes);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = cudaFuncSetAttribute(dit::fmha_fwd_pair_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+  if (e != cudaSuccess) return cuda_fail(e);
+  {
+    cudaLaunchAttribute attr;
+    cudaLaunchConfig_t cfg = pair_launch_config(prop.multiProcessorCount, nullptr, &attr);
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, dit::fmha_fwd_pair_kernel, &cfg);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (clusters < 1) return cuda_fail(cudaErrorInvalidConfiguration);
+    g_state[dev].max_pairs = clusters;
+  }
   g_state[dev].num_sms = prop.multiProcessorCount;
   g_state[dev].ready = true;
   return DIT_ATTN_OK;
@@ -689,15 +782,16 @@ int dit_attn_forward(const void* q, const void* k, const void* v, void* out, int
 
   int dev = -1;
   if (!current_device(&dev)) return DIT_ATTN_ERR_NO_DEVICE;
-  int num_sms;
+  int num_sms, max_pairs;
   {
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_state[dev].ready) return DIT_ATTN_ERR_NOT_INITIALIZED;
     num_sms = g_state[dev].num_sms;
+    max_pairs = g_state[dev].max_pairs;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return d == 64 ? launch<64>(q, k, v, out, BH, Lq, Lk, scale, s, num_sms)
-                 : launch<128>(q, k, v, out, BH, Lq, Lk, scale, s, num_sms);
+                 : launch_pair(q, k, v, out, BH, Lq, Lk, scale, s, max_pairs);
 }
 
 int dit_attn_check_wait_timeout(int limit_us, void* stream) {
