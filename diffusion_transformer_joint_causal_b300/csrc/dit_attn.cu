@@ -205,8 +205,9 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
   constexpr uint32_t hi = desc_hi_sw128(1024);
 #pragma unroll
   for (int k = 0; k < kBN / 16; ++k) {
-    // K step k: 16 keys = 16 rows of 128 bytes; P columns hold bf16 pairs.
-    mma_ts_lo(d_tmem, p_tmem + k * 8, v_lo + ((k * 16 * 128) >> 4), hi, idesc,
+    // K step k: 16 keys = 16 rows of 128 bytes.  P of keys [64h, 64h+64) is in
+    // S columns [64h, 64h+32) as bf16 pairs.
+    mma_ts_lo(d_tmem, p_tmem + (k / 4) * 64 + (k % 4) * 8, v_lo + ((k * 16 * 128) >> 4), hi, idesc,
               (accumulate || k > 0) ? 1u : 0u);
   }
 }
@@ -308,66 +309,73 @@ __device__ void mma_role(const Params& p, const Shared& sh, uint32_t tmem) {
 }
 
 // ----------------------------------------------------------------- softmax + epilogue
-// One thread per query row: thread r of the warpgroup owns TMEM lane r.
+// The eight softmax warps work on one query tile at a time, two threads per
+// query row (TMEM shape 16x32bx2): warp w owns TMEM lanes 32*(w%4) + 16*(w/4)
+// .. +15; lanes 0-15 of the warp take keys 0-63 of the tile and lanes 16-31
+// take keys 64-127 of the same rows.  A half-row's probabilities (32 packed
+// bf16 pairs) go over the first 32 columns of its own 64 S columns, so the two
+// halves never overwrite each other's logits.  Row max, row sum and the
+// recompute decision are combined across the pair with one shuffle.
+
+// O_t row-half rescale: the thread's D/2 output columns times factor.
 template <int D>
-__device__ __forceinline__ void rescale_o(uint32_t taddr_o, float factor) {
+__device__ __forceinline__ void rescale_o_half(uint32_t taddr_o, float factor) {
 #pragma unroll
-  for (int c = 0; c < D / 32; ++c) {
+  for (int c = 0; c < D / 64; ++c) {
     uint32_t o[32];
-    tmem_ld32(taddr_o + c * 32, o);
+    tmem_ld16x2_32<D / 2>(taddr_o + c * 32, o);
     tmem_wait_ld();
 #pragma unroll
     for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * factor);
-    tmem_st32(taddr_o + c * 32, o);
+    tmem_st16x2_32<D / 2>(taddr_o + c * 32, o);
   }
 }
 
-// exp2 of one S tile into packed bf16 probabilities (pk[i] holds keys 2i and
-// 2i+1).  Returns the sum of the probabilities *as rounded to bf16*, so that
-// the row sum l and the P.V product weigh every key identically (a row
-// dominated by one key then returns that key's value row without a
-// rounding-induced scale error); the sum uses mixed-precision f32 += bf16 adds
-// on the packed halves.  kMasked: keys at or beyond `valid` get probability 0.
+// exp2 of 32 keys of a half-row (first key index key0) into 16 packed bf16
+// pairs (pk[i] holds keys key0+2i, key0+2i+1), accumulating into acc[8] the
+// probabilities *as rounded to bf16*, so that the row sum l and the P.V
+// product weigh every key identically (a row dominated by one key then
+// returns that key's value row without a rounding-induced scale error); the
+// sum uses mixed-precision f32 += bf16 adds on the packed halves.
+// kMasked: keys at or beyond `valid` get probability 0.
 template <bool kMasked>
-__device__ __forceinline__ float probs_tile(const uint32_t (&sr)[4][32], float scale_log2,
-                                            float neg_m, int valid, uint32_t (&pk)[64]) {
+__device__ __forceinline__ void probs_chunk(const uint32_t (&sr)[32], float scale_log2, float neg_m,
+                                            int key0, int valid, uint32_t* pk, float (&acc)[8]) {
   const float2 sl2 = make_float2(scale_log2, scale_log2);
   const float2 nm = make_float2(neg_m, neg_m);
-  float acc[8];
 #pragma unroll
-  for (int a = 0; a < 8; ++a) acc[a] = 0.f;
-#pragma unroll
-  for (int c = 0; c < 4; ++c)
-#pragma unroll
-    for (int i = 0; i < 32; i += 2) {
-      const float2 x = __ffma2_rn(
-          make_float2(__uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1])), sl2, nm);
-      float p0 = ex2_approx(x.x);
-      float p1 = ex2_approx(x.y);
-      if (kMasked) {
-        p0 = (c * 32 + i < valid) ? p0 : 0.f;
-        p1 = (c * 32 + i + 1 < valid) ? p1 : 0.f;
-      }
-      const uint32_t w = pack_bf16x2(p0, p1);
-      pk[c * 16 + i / 2] = w;
-      add_bf16x2_halves(acc[(i / 2) & 7], acc[((i / 2) + 4) & 7], w);
+  for (int i = 0; i < 32; i += 2) {
+    const float2 x =
+        __ffma2_rn(make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), sl2, nm);
+    float p0 = ex2_approx(x.x);
+    float p1 = ex2_approx(x.y);
+    if (kMasked) {
+      p0 = (key0 + i < valid) ? p0 : 0.f;
+      p1 = (key0 + i + 1 < valid) ? p1 : 0.f;
     }
+    const uint32_t w = pack_bf16x2(p0, p1);
+    pk[i / 2] = w;
+    add_bf16x2_halves(acc[(i / 2) & 7], acc[((i / 2) + 4) & 7], w);
+  }
+}
+
+__device__ __forceinline__ float sum8(const float (&acc)[8]) {
   return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
 }
 
 template <bool kMasked>
-__device__ __forceinline__ float rowmax_tile(const uint32_t (&sr)[4][32], int valid) {
+__device__ __forceinline__ float rowmax_half(const uint32_t (&sr)[2][32], int key0, int valid) {
   float m[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) m[k] = -INFINITY;
 #pragma unroll
-  for (int c = 0; c < 4; ++c)
+  for (int c = 0; c < 2; ++c)
 #pragma unroll
     for (int i = 0; i < 32; i += 2) {
       float a = __uint_as_float(sr[c][i]), b = __uint_as_float(sr[c][i + 1]);
       if (kMasked) {
-        a = (c * 32 + i < valid) ? a : -INFINITY;
-        b = (c * 32 + i + 1 < valid) ? b : -INFINITY;
+        a = (key0 + c * 32 + i < valid) ? a : -INFINITY;
+        b = (key0 + c * 32 + i + 1 < valid) ? b : -INFINITY;
       }
       m[(c * 16 + i / 2) & 7] = fmax3(m[(c * 16 + i / 2) & 7], a, b);
     }
@@ -375,108 +383,134 @@ __device__ __forceinline__ float rowmax_tile(const uint32_t (&sr)[4][32], int va
 }
 
 // kPair: the CTA is one half of a pair; a work unit then spans 512 query rows
-// (this CTA's 256 start at rank*256) and P-ready is reported, one arrival per
-// warp, on the barrier of the pair's leader CTA, whose warp issues the MMAs.
+// (this CTA's 256 start at rank*256) and P-ready is reported on the barrier of
+// the pair's leader CTA, whose warp issues the MMAs.  Each warp arrives once
+// per tile (after its TMEM stores completed).
 template <int D, class T, bool kPair>
-__device__ void softmax_role(const Params& p, const Shared& sh, uint32_t tmem, int t) {
-  const int wg_warp = (threadIdx.x / 32) & 3;
-  const int r = wg_warp * 32 + (threadIdx.x & 31);   // row within the query tile
-  const uint32_t lane_base = tmem + (static_cast<uint32_t>(wg_warp * 32) << 16);
-  const uint32_t taddr_s = lane_base + T::col_s(t);
-  const uint32_t taddr_o = lane_base + T::col_o(t);
+__device__ void softmax_role(const Params& p, const Shared& sh, uint32_t tmem) {
+  const int warp = threadIdx.x / 32;                 // 0..7
+  const int lane = threadIdx.x & 31;
+  const int half = lane >> 4;                        // keys [64*half, 64*half + 64) of a tile
+  const int lane0 = (warp & 3) * 32 + (warp >> 2) * 16;
+  const int r = lane0 + (lane & 15);                 // row within a query tile
+  const uint32_t lane_addr = tmem + (static_cast<uint32_t>(lane0) << 16);
   const float scale_log2 = p.scale_log2;
   const int n_kv = (p.Lk + kBN - 1) / kBN;
-  const int tail = p.Lk - (n_kv - 1) * kBN;   // valid keys in the last tile, 1..128
+  const int tail = p.Lk - (n_kv - 1) * kBN;          // valid keys in the last tile, 1..128
+  const int key0 = 64 * half;
   uint32_t g = 0, it = 0;
   bool ok = true;
   const int rank = kPair ? static_cast<int>(cluster_ctarank()) : 0;
   const int u0 = kPair ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
   const int u_stride = kPair ? static_cast<int>(num_clusters_x()) : static_cast<int>(gridDim.x);
   const int unit_rows = kPair ? 2 * kUnitRows : kUnitRows;
-  const uint32_t p_full_leader = kPair ? mapa_shared(sh.bar(T::kBarPFull + t), 0) : 0u;
+  const uint32_t p_full_leader0 = kPair ? mapa_shared(sh.bar(T::kBarPFull), 0) : 0u;
 
   for (int u = u0; u < p.num_units && ok; u += u_stride, ++it) {
     const int bh = u / p.num_qblocks;
-    const int row = (u % p.num_qblocks) * unit_rows + rank * kUnitRows + t * kBM + r;
-    float m_used = -INFINITY;   // running max, in units of s*scale*log2(e)
-    float l = 0.f;
-    for (int j = 0; j < n_kv; ++j, ++g) {
-      const bool got = mbar_wait(sh.bar(T::kBarSFull + t), g & 1u, kWaitLimitNs, sh.abort);
-      if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(taddr_s + c * 32, sr[c]);
-      tmem_wait_ld();
+    const int row_base = (u % p.num_qblocks) * unit_rows + rank * kUnitRows + r;
+    float m_used[2] = {-INFINITY, -INFINITY};   // running max, in units of s*scale*log2(e)
+    float l[2] = {0.f, 0.f};                     // this half-row's share of the row sum
+    for (int j = 0; j < n_kv && ok; ++j, ++g) {
       const bool masked = (j == n_kv - 1) && (tail < kBN);
       const int valid = masked ? tail : kBN;
-      uint32_t pk[64];
-      float tile_sum;
-      // Row max, lazy rescale of l and O, probabilities (first tile, or a redo).
-      auto max_pass = [&]() {
-        const float mx = masked ? rowmax_tile<true>(sr, tail) : rowmax_tile<false>(sr, kBN);
-        const float m_tile = mx * scale_log2;
-        float factor = 1.f;
-        if (m_tile > m_used + kRescaleThreshold) {
-          factor = ex2_approx(m_used - m_tile);   // 0 on the first tile
-          l *= factor;
-          m_used = m_tile;
-        }
-        // O_t is quiescent here: S_t's completion implies the previous P.V product finished.
-        if (j > 0 && __any_sync(0xffffffffu, factor != 1.f)) rescale_o<D>(taddr_o, factor);
-        return masked ? probs_tile<true>(sr, scale_log2, -m_used, valid, pk)
-                      : probs_tile<false>(sr, scale_log2, -m_used, kBN, pk);
-      };
-      if (j == 0) {
-        tile_sum = max_pass();
-      } else {
-        // Optimistic pass against the running max.  A tile whose rounded sum
-        // exceeds 2^16 has some p > 2^9: it reloads S (still intact in TMEM,
-        // P is not stored yet), raises the max (always, since p > 2^8),
-        // rescales l and O and recomputes.  Warp-uniform branch: the TMEM
-        // accesses stay collective.
-        tile_sum = masked ? probs_tile<true>(sr, scale_log2, -m_used, valid, pk)
-                          : probs_tile<false>(sr, scale_log2, -m_used, kBN, pk);
-        if (__any_sync(0xffffffffu, !(tile_sum <= kOptimisticSumLimit))) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_ld32(taddr_s + c * 32, sr[c]);
+      for (int t = 0; t < 2; ++t) {
+        const bool got = mbar_wait(sh.bar(T::kBarSFull + t), g & 1u, kWaitLimitNs, sh.abort);
+        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t taddr_s = lane_addr + T::col_s(t);
+        const uint32_t taddr_o = lane_addr + T::col_o(t);
+        // Logits stay in registers for the whole tile; the second chunk's TMEM
+        // load and the first chunk's P store overlap with arithmetic.  P goes
+        // over this half-row's own first 32 S columns; a recompute overwrites
+        // it before P-ready is signalled.
+        uint32_t sr[2][32];
+        uint32_t pk[32];
+        float acc[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) acc[a] = 0.f;
+        tmem_ld16x2_32<64>(taddr_s, sr[0]);
+        tmem_wait_ld();
+        tmem_ld16x2_32<64>(taddr_s + 32, sr[1]);
+        // probabilities of chunk c against the running max m, packed and stored
+        auto chunk = [&](int c, float m) {
+          if (masked) probs_chunk<true>(sr[c], scale_log2, -m, key0 + 32 * c, valid, &pk[16 * c], acc);
+          else probs_chunk<false>(sr[c], scale_log2, -m, key0 + 32 * c, kBN, &pk[16 * c], acc);
+          tmem_st16x2_16<64>(taddr_s + 16 * c, &pk[16 * c]);
+        };
+        // Row max over both halves, lazy rescale of l and O, probabilities
+        // (first tile, or a recompute).
+        auto max_pass = [&]() {
+          tmem_wait_st();   // earlier optimistic P stores land before they are overwritten
+          float mx = masked ? rowmax_half<true>(sr, key0, valid) : rowmax_half<false>(sr, key0, kBN);
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float m_tile = mx * scale_log2;
+          float factor = 1.f;
+          if (m_tile > m_used[t] + kRescaleThreshold) {
+            factor = ex2_approx(m_used[t] - m_tile);   // 0 on the first tile
+            l[t] *= factor;
+            m_used[t] = m_tile;
+          }
+          // O_t is quiescent: S_t's completion implies the previous P.V product finished.
+          if (j > 0 && __any_sync(0xffffffffu, factor != 1.f)) rescale_o_half<D>(taddr_o, factor);
+#pragma unroll
+          for (int a = 0; a < 8; ++a) acc[a] = 0.f;
+          chunk(0, m_used[t]);
+          chunk(1, m_used[t]);
+        };
+        if (j == 0) {
           tmem_wait_ld();
-          tile_sum = max_pass();
+          max_pass();
+        } else {
+          // Optimistic pass against the running max.  If a row's rounded sum
+          // exceeds 2^16, some p > 2^9: the row raises its max (always, since
+          // p > 2^8), rescales l and O and recomputes.  Warp-uniform branch.
+          chunk(0, m_used[t]);
+          tmem_wait_ld();
+          chunk(1, m_used[t]);
+          const float half_sum = sum8(acc);
+          const float row_sum = half_sum + __shfl_xor_sync(0xffffffffu, half_sum, 16);
+          if (__any_sync(0xffffffffu, !(row_sum <= kOptimisticSumLimit))) max_pass();
         }
-      }
-      l += tile_sum;
-      tmem_st32(taddr_s, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
-      tmem_st32(taddr_s + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
-      tmem_wait_st();
-      tc_fence_before();
-      if (kPair) {
+        l[t] += sum8(acc);
+        tmem_wait_st();
+        tc_fence_before();
         __syncwarp();
-        if ((threadIdx.x & 31) == 0) mbar_arrive_cluster(p_full_leader);
-      } else {
-        mbar_arrive(sh.bar(T::kBarPFull + t));
+        if (lane == 0) {
+          if (kPair) mbar_arrive_cluster(p_full_leader0 + 8u * t);
+          else mbar_arrive(sh.bar(T::kBarPFull + t));
+        }
       }
     }
     if (!ok) break;
-    // Epilogue: O_t / l -> bf16 -> global, one contiguous row per thread.
-    const bool got = mbar_wait(sh.bar(T::kBarOFull + t), it & 1u, kWaitLimitNs, sh.abort);
-    if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-    tc_fence_after();
-    const float inv_l = 1.f / l;
-    const bool row_ok = row < p.Lq;
-    uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(bh) * p.Lq + row) * D);
+    // Epilogue: O_t / l -> bf16 -> global; each thread writes its D/2 columns.
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t o[32];
-      tmem_ld32(taddr_o + c * 32, o);
-      tmem_wait_ld();
-      uint32_t w[16];
+    for (int t = 0; t < 2; ++t) {
+      const bool got = mbar_wait(sh.bar(T::kBarOFull + t), it & 1u, kWaitLimitNs, sh.abort);
+      if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+      tc_fence_after();
+      const float l_row = l[t] + __shfl_xor_sync(0xffffffffu, l[t], 16);
+      const float inv_l = 1.f / l_row;
+      const int row = row_base + t * kBM;
+      const bool row_ok = row < p.Lq;
+      uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(bh) * p.Lq + row) * D +
+                                            half * (D / 2));
+      const uint32_t taddr_o = lane_addr + T::col_o(t);
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-      if (row_ok) {
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t o[32];
+        tmem_ld16x2_32<D / 2>(taddr_o + c * 32, o);
+        tmem_wait_ld();
+        uint32_t w[16];
 #pragma unroll
-        for (int v = 0; v < 4; ++v)
-          dst[c * 4 + v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+        if (row_ok) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[c * 4 + v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+        }
       }
     }
   }
@@ -510,7 +544,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       mbar_init(sh.bar(T::kBarQFull + t), 1);
       mbar_init(sh.bar(T::kBarQEmpty + t), 1);
       mbar_init(sh.bar(T::kBarSFull + t), 1);
-      mbar_init(sh.bar(T::kBarPFull + t), kBM);
+      mbar_init(sh.bar(T::kBarPFull + t), 8);   // one arrival per softmax warp
       mbar_init(sh.bar(T::kBarOFull + t), 1);
     }
     mbar_init(sh.bar(T::kBarDrain), 1);
@@ -533,7 +567,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
   if (warp < kMmaWarp) {
     reg_alloc<kRegsSoftmax>();
-    softmax_role<D, Traits<D>, false>(p, sh, tmem, warp / 4);
+    softmax_role<D, Traits<D>, false>(p, sh, tmem);
   } else if (warp == kMmaWarp) {
     reg_dealloc<kRegsOther>();
     mma_role<D>(p, sh, tmem);

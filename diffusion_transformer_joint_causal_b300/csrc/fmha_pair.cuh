@@ -39,13 +39,13 @@ struct PairTraits {
   static constexpr int kBarQFull = 2 * kStages;      // leader: both CTAs' query tile t landed
   static constexpr int kBarQEmpty = kBarQFull + 2;   // both
   static constexpr int kBarSFull = kBarQEmpty + 2;   // both
-  static constexpr int kBarPFull = kBarSFull + 2;    // leader: 8 warp arrivals
+  static constexpr int kBarPFull = kBarSFull + 2;    // leader: 16 warp arrivals
   static constexpr int kBarOFull = kBarPFull + 2;    // both
   static constexpr int kBarDrain = kBarOFull + 2;    // leader
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = 1024 + kOffMisc + 16;
-  static constexpr uint32_t kPFullArrivals = 8;      // 4 warps x 2 CTAs
+  static constexpr uint32_t kPFullArrivals = 16;     // 8 softmax warps x 2 CTAs
 };
 
 // ----------------------------------------------------------------- producer (both CTAs)
@@ -153,9 +153,9 @@ __device__ __forceinline__ void pair_issue_pv(uint32_t d_tmem, uint32_t p_tmem, 
   constexpr uint32_t idesc = idesc_bf16_f32(2 * kBM, PairTraits::D, 0, 1);
   constexpr uint32_t hi = desc_hi_sw128(1024);
 #pragma unroll
-  for (int k = 0; k < kBN / 16; ++k)
-    mma_ts_lo_pair(d_tmem, p_tmem + k * 8, v_lo + ((k * 16 * 128) >> 4), hi, idesc,
-                   (accumulate || k > 0) ? 1u : 0u);
+  for (int k = 0; k < kBN / 16; ++k)   // P of keys [64h, 64h+64) is in S columns [64h, 64h+32)
+    mma_ts_lo_pair(d_tmem, p_tmem + (k / 4) * 64 + (k % 4) * 8, v_lo + ((k * 16 * 128) >> 4), hi,
+                   idesc, (accumulate || k > 0) ? 1u : 0u);
 }
 
 __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) {
@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
   if (warp < kMmaWarp) {
     reg_alloc<kRegsSoftmax>();
-    softmax_role<T::D, T, true>(p, sh, tmem, warp / 4);
+    softmax_role<T::D, T, true>(p, sh, tmem);
   } else if (warp == kMmaWarp) {
     reg_dealloc<kRegsOther>();
     if (leader) pair_mma_role(p, sh, tmem);
