@@ -382,6 +382,70 @@ __device__ __forceinline__ float rowmax_half(const uint32_t (&sr)[2][32], int ke
   return fmaxf(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], fmax3(m[5], m[6], m[7])));
 }
 
+// One query tile's softmax step for this thread's half-row (keys key0 ..
+// key0+63 of the tile): loads the logits from TMEM at taddr_s, updates the
+// running max m_used and this half-row's share of the row sum l, calls
+// o_rescale(factor) when the max rises (the hook must scale this thread's
+// half of every O accumulator of the row, once no P.V product still writes
+// them), and writes the packed bf16 probabilities over the half-row's first
+// 32 S columns.  Returns after issuing the TMEM stores (the caller waits).
+template <int D, class ORescale>
+__device__ __forceinline__ void softmax_tile_half(uint32_t taddr_s, int key0, bool first,
+                                                  bool masked, int valid, float scale_log2,
+                                                  float& m_used, float& l, ORescale&& o_rescale) {
+  // Logits stay in registers for the whole tile; the second chunk's TMEM
+  // load and the first chunk's P store overlap with arithmetic.  A recompute
+  // overwrites P before P-ready is signalled.
+  uint32_t sr[2][32];
+  uint32_t pk[32];
+  float acc[8];
+#pragma unroll
+  for (int a = 0; a < 8; ++a) acc[a] = 0.f;
+  tmem_ld16x2_32<64>(taddr_s, sr[0]);
+  tmem_wait_ld();
+  tmem_ld16x2_32<64>(taddr_s + 32, sr[1]);
+  // probabilities of chunk c against the running max m, packed and stored
+  auto chunk = [&](int c, float m) {
+    if (masked) probs_chunk<true>(sr[c], scale_log2, -m, key0 + 32 * c, valid, &pk[16 * c], acc);
+    else probs_chunk<false>(sr[c], scale_log2, -m, key0 + 32 * c, kBN, &pk[16 * c], acc);
+    tmem_st16x2_16<64>(taddr_s + 16 * c, &pk[16 * c]);
+  };
+  // Row max over both halves, lazy rescale of l and O, probabilities
+  // (first tile, or a recompute).
+  auto max_pass = [&]() {
+    tmem_wait_st();   // earlier optimistic P stores land before they are overwritten
+    float mx = masked ? rowmax_half<true>(sr, key0, valid) : rowmax_half<false>(sr, key0, kBN);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    const float m_tile = mx * scale_log2;
+    float factor = 1.f;
+    if (m_tile > m_used + kRescaleThreshold) {
+      factor = ex2_approx(m_used - m_tile);   // 0 on the first tile
+      l *= factor;
+      m_used = m_tile;
+    }
+    if (!first && __any_sync(0xffffffffu, factor != 1.f)) o_rescale(factor);
+#pragma unroll
+    for (int a = 0; a < 8; ++a) acc[a] = 0.f;
+    chunk(0, m_used);
+    chunk(1, m_used);
+  };
+  if (first) {
+    tmem_wait_ld();
+    max_pass();
+  } else {
+    // Optimistic pass against the running max.  If a row's rounded sum
+    // exceeds 2^16, some p > 2^9: the row raises its max (always, since
+    // p > 2^8), rescales l and O and recomputes.  Warp-uniform branch.
+    chunk(0, m_used);
+    tmem_wait_ld();
+    chunk(1, m_used);
+    const float half_sum = sum8(acc);
+    const float row_sum = half_sum + __shfl_xor_sync(0xffffffffu, half_sum, 16);
+    if (__any_sync(0xffffffffu, !(row_sum <= kOptimisticSumLimit))) max_pass();
+  }
+  l += sum8(acc);
+}
+
 // kPair: the CTA is one half of a pair; a work unit then spans 512 query rows
 // (this CTA's 256 start at rank*256) and P-ready is reported on the barrier of
 // the pair's leader CTA, whose warp issues the MMAs.  Each warp arrives once
@@ -419,61 +483,11 @@ __device__ void softmax_role(const Params& p, const Shared& sh, uint32_t tmem) {
         const bool got = mbar_wait(sh.bar(T::kBarSFull + t), g & 1u, kWaitLimitNs, sh.abort);
         if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t taddr_s = lane_addr + T::col_s(t);
+        // O_t is quiescent here: S_t's completion implies the previous P.V
+        // product into O_t finished.
         const uint32_t taddr_o = lane_addr + T::col_o(t);
-        // Logits stay in registers for the whole tile; the second chunk's TMEM
-        // load and the first chunk's P store overlap with arithmetic.  P goes
-        // over this half-row's own first 32 S columns; a recompute overwrites
-        // it before P-ready is signalled.
-        uint32_t sr[2][32];
-        uint32_t pk[32];
-        float acc[8];
-#pragma unroll
-        for (int a = 0; a < 8; ++a) acc[a] = 0.f;
-        tmem_ld16x2_32<64>(taddr_s, sr[0]);
-        tmem_wait_ld();
-        tmem_ld16x2_32<64>(taddr_s + 32, sr[1]);
-        // probabilities of chunk c against the running max m, packed and stored
-        auto chunk = [&](int c, float m) {
-          if (masked) probs_chunk<true>(sr[c], scale_log2, -m, key0 + 32 * c, valid, &pk[16 * c], acc);
-          else probs_chunk<false>(sr[c], scale_log2, -m, key0 + 32 * c, kBN, &pk[16 * c], acc);
-          tmem_st16x2_16<64>(taddr_s + 16 * c, &pk[16 * c]);
-        };
-        // Row max over both halves, lazy rescale of l and O, probabilities
-        // (first tile, or a recompute).
-        auto max_pass = [&]() {
-          tmem_wait_st();   // earlier optimistic P stores land before they are overwritten
-          float mx = masked ? rowmax_half<true>(sr, key0, valid) : rowmax_half<false>(sr, key0, kBN);
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-          const float m_tile = mx * scale_log2;
-          float factor = 1.f;
-          if (m_tile > m_used[t] + kRescaleThreshold) {
-            factor = ex2_approx(m_used[t] - m_tile);   // 0 on the first tile
-            l[t] *= factor;
-            m_used[t] = m_tile;
-          }
-          // O_t is quiescent: S_t's completion implies the previous P.V product finished.
-          if (j > 0 && __any_sync(0xffffffffu, factor != 1.f)) rescale_o_half<D>(taddr_o, factor);
-#pragma unroll
-          for (int a = 0; a < 8; ++a) acc[a] = 0.f;
-          chunk(0, m_used[t]);
-          chunk(1, m_used[t]);
-        };
-        if (j == 0) {
-          tmem_wait_ld();
-          max_pass();
-        } else {
-          // Optimistic pass against the running max.  If a row's rounded sum
-          // exceeds 2^16, some p > 2^9: the row raises its max (always, since
-          // p > 2^8), rescales l and O and recomputes.  Warp-uniform branch.
-          chunk(0, m_used[t]);
-          tmem_wait_ld();
-          chunk(1, m_used[t]);
-          const float half_sum = sum8(acc);
-          const float row_sum = half_sum + __shfl_xor_sync(0xffffffffu, half_sum, 16);
-          if (__any_sync(0xffffffffu, !(row_sum <= kOptimisticSumLimit))) max_pass();
-        }
-        l[t] += sum8(acc);
+        softmax_tile_half<D>(lane_addr + T::col_s(t), key0, j == 0, masked, valid, scale_log2,
+                             m_used[t], l[t], [&](float f) { rescale_o_half<D>(taddr_o, f); });
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -686,11 +700,12 @@ int launch(const void* q, const void* k, const void* v, void* out, int64_t BH, i
   return DIT_ATTN_OK;
 }
 
-cudaLaunchConfig_t pair_launch_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr) {
+cudaLaunchConfig_t pair_launch_config(int grid, cudaStream_t stream, cudaLaunchAttribute* attr,
+                                      uint32_t smem_bytes = dit::PairTraits::kSmemBytes) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(dit::kNumThreads, 1, 1);
-  cfg.dynamicSmemBytes = dit::PairTraits::kSmemBytes;
+  cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = stream;
   attr->id = cudaLaunchAttributeClusterDimension;
   attr->val.clusterDim.x = 2;
