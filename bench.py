@@ -57,6 +57,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target duration of the oracle's CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the per-workload timing sweep (eager and CUDA-graph replay)")
     return ap.parse_args()
 
 
@@ -325,6 +327,49 @@ def bench_reference(args):
     return 0
 
 
+def workload_sweep(dit, dev, calls: int = 20):
+    """Per-workload time per call: eager launches and one CUDA graph replaying
+    the same `calls` launches (inputs resident, CUDA events)."""
+    import numpy as np
+    import torch
+
+    import workloads as W
+    res = {}
+    for w in W.WORKLOADS:
+        q, k, v = (torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+                   for x in W.make_qkv(w))
+        out = torch.empty_like(q)
+        for _ in range(3):
+            dit.forward(q, k, v, w.scale, out=out)
+        s = torch.cuda.Stream(dev)
+        s.wait_stream(torch.cuda.current_stream(dev))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(calls):
+                    dit.forward(q, k, v, w.scale, out=out)
+        g.replay()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(calls):
+            dit.forward(q, k, v, w.scale, out=out)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        eager = e0.elapsed_time(e1) / calls
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        graph = e0.elapsed_time(e1) / calls
+        res[w.name] = {"shape": [w.B, w.H, w.Lq, w.Lk, w.d], "ms_eager": eager,
+                       "ms_graph": graph, "tflops_eager": w.flops / eager / 1e9,
+                       "tflops_graph": w.flops / graph / 1e9}
+        del q, k, v, out, g
+        torch.cuda.empty_cache()
+    return res
+
+
 def bench_ours(args):
     import numpy as np
     import torch
@@ -436,6 +481,8 @@ def bench_ours(args):
         "gpu_launches": args.steps,
         "clocks": sampler.summary(),
     }
+    if world == 1 and not args.no_sweep:
+        line["per_workload"] = workload_sweep(dit, dev)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     print(json.dumps(line), flush=True)
