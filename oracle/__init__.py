@@ -12,7 +12,10 @@ definition of standard attention (the dense BF16 attention that "Speed Up
 Image Generation with FLUX 3 Image Klein on NVIDIA Blackwell GPUs", Key
 takeaways, second item, measures): o_i = sum_j softmax_j(scale * q_i . k_j) v_j.
 
-Pins (tests/test_oracle_pins.py) tie it to things other than itself: a
+It also holds the RMS normalisation of queries and keys (``rmsnorm``) that the
+normalised workloads apply before attention.
+
+Pins (tests/test_oracle_pins.py, tests/test_rmsnorm_oracle.py) tie it to things other than itself: a
 50-digit decimal brute force on tiny inputs, the two-key sigmoid closed form,
 exact special cases (constant V, Lk = 1, scale = 0, one-hot selection), key /
 query permutation equivariance, key-shift invariance and the convex-hull bound.
@@ -60,6 +63,10 @@ def _load():
                           ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                           ctypes.c_double, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+            g = lib.oracle_rmsnorm
+            g.restype = ctypes.c_int
+            g.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                          ctypes.c_int64, ctypes.c_double, ctypes.c_void_p]
             _lib = lib
     return _lib
 
@@ -123,3 +130,25 @@ def attention(q, k, v, scale: float, n_threads: int | None = None,
         o, p = res
         return o.reshape(B, H, Lq, d), p.reshape(B, H, Lq, Lk)
     return res.reshape(B, H, Lq, d)
+
+
+def rmsnorm(x, weight=None, eps: float = 1e-6):
+    """y = x / sqrt(mean(x^2 over the last axis) + eps) * weight, float64.
+
+    x: [..., d] uint16 bf16 bits or float64; weight: [d] of the same kind or None.
+    """
+    x, kx = _prep(x)
+    shape = x.shape
+    d = shape[-1]
+    rows = int(np.prod(shape[:-1])) if len(shape) > 1 else 1
+    w = None
+    if weight is not None:
+        w, kw = _prep(weight)
+        if kw != kx or w.shape != (d,):
+            raise ValueError("weight must be [d] of the same element type as x")
+    y = np.empty(shape, dtype=np.float64)
+    rc = _load().oracle_rmsnorm(x.ctypes.data, w.ctypes.data if w is not None else None, kx,
+                                rows, d, float(eps), y.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle_rmsnorm rejected its arguments")
+    return y

@@ -142,3 +142,31 @@ int oracle_attention_rows(const void *q, const void *k, const void *v, int kind,
     free(tid);
     return status;
 }
+
+/*
+ * oracle_rmsnorm: y[r, c] = x[r, c] / sqrt(mean_c' x[r, c']^2 + eps) * w[c]
+ * for every row r, in double precision (w = 1 when weight is NULL).
+ *   x: [rows, d] (kind 0: uint16 bf16 bits, 1: double); weight: same kind or NULL
+ *   y: [rows, d] doubles.  Returns 0, or -1 on bad arguments.
+ * This is the per-token, per-head RMS normalisation of queries and keys that
+ * the normalised workloads apply before attention.
+ */
+int oracle_rmsnorm(const void *x, const void *weight, int kind, int64_t rows, int64_t d,
+                   double eps, double *y)
+{
+    if (!x || !y || rows < 1 || d < 1 || !(eps >= 0.0)) return -1;
+    if (kind != ORACLE_BF16 && kind != ORACLE_F64) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        double ss = 0.0;
+        for (int64_t c = 0; c < d; ++c) {
+            const double v = load_elem(x, kind, r * d + c);
+            ss += v * v;
+        }
+        const double inv = 1.0 / sqrt(ss / (double)d + eps);
+        for (int64_t c = 0; c < d; ++c) {
+            const double w = weight ? load_elem(weight, kind, c) : 1.0;
+            y[r * d + c] = load_elem(x, kind, r * d + c) * inv * w;
+        }
+    }
+    return 0;
+}
