@@ -370,6 +370,30 @@ def workload_sweep(dit, dev, calls: int = 20):
     return res
 
 
+def rmsnorm_roofline(dit, dev, peaks, calls: int = 20):
+    """RMS normalisation of the 2048x2048 T2I query tensor (B*H*L = 811008 rows,
+    d = 128): HBM-bound, algorithmic bytes = read + write of every element."""
+    import torch
+    rows, d = 2 * 24 * 16896, 128
+    x = torch.randn(rows, d, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    y = torch.empty_like(x)
+    for _ in range(3):
+        dit.rmsnorm(x, out=y)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(calls):
+        dit.rmsnorm(x, out=y)
+    e1.record()
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / calls
+    nbytes = 2.0 * rows * d * 2
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"rows": rows, "d": d, "ms_per_call": ms, "algorithmic_bytes": nbytes,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm"], "peak_source": f"{peaks['source']} copy"}}
+
+
 def bench_ours(args):
     import numpy as np
     import torch
@@ -483,6 +507,7 @@ def bench_ours(args):
     }
     if world == 1 and not args.no_sweep:
         line["per_workload"] = workload_sweep(dit, dev)
+        line["rmsnorm_qk_prologue"] = rmsnorm_roofline(dit, dev, peaks)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     print(json.dumps(line), flush=True)

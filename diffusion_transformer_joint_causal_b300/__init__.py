@@ -18,7 +18,7 @@ import os
 import threading
 
 __all__ = ["create", "destroy", "forward", "forward_ptr", "status_string", "get_device_error",
-           "check_wait_timeout",
+           "check_wait_timeout", "rmsnorm", "rmsnorm_ptr",
            "last_cuda_error", "version", "library_path", "DitAttnError", "STATUS",
            "EXPORTED_SYMBOLS"]
 
@@ -32,7 +32,7 @@ STATUS = {
 
 EXPORTED_SYMBOLS = ("dit_attn_version", "dit_attn_create", "dit_attn_forward",
                     "dit_attn_destroy", "dit_attn_status_string", "dit_attn_get_device_error",
-                    "dit_attn_check_wait_timeout", "dit_attn_last_cuda_error")
+                    "dit_attn_check_wait_timeout", "dit_attn_last_cuda_error", "dit_attn_rmsnorm")
 
 _lock = threading.Lock()
 _lib = None
@@ -75,6 +75,8 @@ def _load():
             lib.dit_attn_get_device_error.argtypes = [vp]
             lib.dit_attn_check_wait_timeout.restype = c_int
             lib.dit_attn_check_wait_timeout.argtypes = [c_int, vp]
+            lib.dit_attn_rmsnorm.restype = c_int
+            lib.dit_attn_rmsnorm.argtypes = [vp, vp, vp, ctypes.c_longlong, c_int, ctypes.c_float, vp]
             lib.dit_attn_last_cuda_error.restype = c_int
             lib.dit_attn_last_cuda_error.argtypes = []
             _lib = lib
@@ -163,4 +165,36 @@ def forward(q, k, v, scale: float | None = None, out=None, stream=None):
                          B, H, Lq, Lk, d, float(scale), _stream_handle(stream))
     if rc:
         raise DitAttnError(rc, "dit_attn_forward")
+    return out
+
+
+def rmsnorm_ptr(x: int, y: int, weight: int, rows: int, d: int, eps: float, stream=0) -> int:
+    """Raw C-ABI call of dit_attn_rmsnorm with integer device pointers; returns the status."""
+    s = stream if isinstance(stream, ctypes.c_void_p) else ctypes.c_void_p(int(stream))
+    return _load().dit_attn_rmsnorm(ctypes.c_void_p(x), ctypes.c_void_p(y),
+                                    ctypes.c_void_p(weight) if weight else None,
+                                    ctypes.c_longlong(rows), d, ctypes.c_float(eps), s)
+
+
+def rmsnorm(x, weight=None, eps: float = 1e-6, out=None, stream=None):
+    """out = bf16(x / sqrt(mean(x^2, last dim) + eps) * weight) for a bf16 CUDA tensor
+    whose last dimension (64 or 128) is the head dimension; ``out=x`` works in place."""
+    import torch
+    if not isinstance(x, torch.Tensor) or x.dtype != torch.bfloat16 or not x.is_cuda:
+        raise TypeError("x must be a bfloat16 CUDA tensor")
+    if not x.is_contiguous() or x.dim() < 1:
+        raise ValueError("x must be contiguous")
+    d = x.shape[-1]
+    if weight is not None and (weight.dtype != torch.bfloat16 or tuple(weight.shape) != (d,)
+                               or not weight.is_contiguous() or weight.device != x.device):
+        raise ValueError("weight must be a contiguous bf16 [d] tensor on x's device")
+    if out is None:
+        out = torch.empty_like(x)
+    elif out.dtype != torch.bfloat16 or out.shape != x.shape or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like x")
+    with torch.cuda.device(x.device):
+        rc = rmsnorm_ptr(x.data_ptr(), out.data_ptr(), weight.data_ptr() if weight is not None else 0,
+                         x.numel() // d, d, float(eps), _stream_handle(stream))
+    if rc:
+        raise DitAttnError(rc, "dit_attn_rmsnorm")
     return out

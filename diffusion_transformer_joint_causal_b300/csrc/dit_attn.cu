@@ -620,6 +620,7 @@ __global__ void wait_timeout_kernel(uint64_t limit_ns) {
 }  // namespace dit
 
 #include "fmha_pair.cuh"
+#include "rmsnorm.cuh"
 
 // =================================================================== host side
 namespace {
@@ -853,6 +854,41 @@ int dit_attn_check_wait_timeout(int limit_us, void* stream) {
   }
   dit::wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<uint64_t>(limit_us) * 1000ull);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return DIT_ATTN_OK;
+}
+
+int dit_attn_rmsnorm(const void* x, void* y, const void* weight, long long rows, int d, float eps,
+                     void* stream) {
+  if (!x || !y) return DIT_ATTN_ERR_INVALID_ARG;
+  if (rows < 1 || !std::isfinite(eps) || eps < 0.f) return DIT_ATTN_ERR_INVALID_ARG;
+  const uintptr_t mis = reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y) |
+                        reinterpret_cast<uintptr_t>(weight);
+  if (mis & 15u) return DIT_ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return DIT_ATTN_ERR_UNSUPPORTED;
+  if (rows > (static_cast<long long>(1) << 40)) return DIT_ATTN_ERR_UNSUPPORTED;
+  const int64_t bytes = static_cast<int64_t>(rows) * d * 2;
+  if (x != y && overlaps(x, bytes, y, bytes)) return DIT_ATTN_ERR_INVALID_ARG;
+  if (weight && (overlaps(weight, d * 2, y, bytes))) return DIT_ATTN_ERR_INVALID_ARG;
+  int dev = -1;
+  if (!current_device(&dev)) return DIT_ATTN_ERR_NO_DEVICE;
+  int num_sms;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_state[dev].ready) return DIT_ATTN_ERR_NOT_INITIALIZED;
+    num_sms = g_state[dev].num_sms;
+  }
+  const int rows_per_block = 8 * (32 / (d / 8)) * 4;
+  const int64_t want = (static_cast<int64_t>(rows) + rows_per_block - 1) / rows_per_block;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  const int grid = static_cast<int>(want < cap ? want : cap);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint4* xv = static_cast<const uint4*>(x);
+  uint4* yv = static_cast<uint4*>(y);
+  const uint4* wv = static_cast<const uint4*>(weight);
+  if (d == 64) dit::rmsnorm_kernel<64><<<grid, 256, 0, s>>>(xv, yv, wv, rows, eps);
+  else dit::rmsnorm_kernel<128><<<grid, 256, 0, s>>>(xv, yv, wv, rows, eps);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   return DIT_ATTN_OK;

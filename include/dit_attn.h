@@ -75,6 +75,22 @@ int dit_attn_create(void);
 int dit_attn_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int Lq,
                      int Lk, int d, float scale, void* stream);
 
+/*
+ * RMS normalisation of queries or keys over the head dimension, per token and
+ * head (the normalisation the 1024x1024 and 2048x2048 workloads apply to Q
+ * and K before attention; the pages do not print it, so no weight is implied):
+ *
+ *     y[r, :] = bf16( x[r, :] / sqrt(mean_c x[r, c]^2 + eps) * weight[:] )
+ *
+ * computed in fp32, rounded to nearest-even bf16.  x and y: device pointers,
+ * bf16, contiguous [rows, d] (a [B, H, L, d] tensor is rows = B*H*L); y may
+ * equal x (in place) but must not otherwise overlap it.  weight: NULL (all
+ * ones) or a device bf16 [d].  d in {64, 128}; rows >= 1; eps finite, >= 0.
+ * Pointers 16-byte aligned.  Enqueued on `stream`; requires dit_attn_create().
+ */
+int dit_attn_rmsnorm(const void* x, void* y, const void* weight, long long rows, int d, float eps,
+                     void* stream);
+
 /* Forget the current device's state; forward then returns NOT_INITIALIZED. */
 int dit_attn_destroy(void);
 

@@ -103,3 +103,23 @@ def test_wait_timeout_check_validates_before_cuda():
     lib = ctypes.CDLL(dit.library_path())
     assert lib.dit_attn_check_wait_timeout(0, None) == 1
     assert lib.dit_attn_check_wait_timeout(2000000, None) == 1
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((0, A, 0, 8, 128, 1e-6), 1),                    # null x
+    ((A, 0, 0, 8, 128, 1e-6), 1),                    # null y
+    ((A, A + MB, 0, 0, 128, 1e-6), 1),               # rows = 0
+    ((A, A + MB, 0, 8, 128, -1.0), 1),               # negative eps
+    ((A, A + MB, 0, 8, 128, float("nan")), 1),       # NaN eps
+    ((A + 4, A + MB, 0, 8, 128, 1e-6), 1),           # misaligned x
+    ((A, A + MB, A + 2 * MB + 8, 8, 128, 1e-6), 1),  # misaligned weight
+    ((A, A + 512, 0, 8, 128, 1e-6), 1),              # partial overlap of x and y
+    ((A, A + MB, 0, 8, 96, 1e-6), 2),                # d = 96
+])
+def test_rmsnorm_rejects_bad_arguments(args, expect):
+    assert dit.rmsnorm_ptr(*args) == expect
+
+
+@pytest.mark.skipif(_has_gpu(), reason="checks the no-device path")
+def test_rmsnorm_no_device():
+    assert dit.rmsnorm_ptr(A, A, 0, 8, 128, 1e-6) == 4      # in place is allowed
