@@ -27,6 +27,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import sys
@@ -42,6 +43,7 @@ FALLBACK_PEAK_TFLOPS = 1800.0
 FALLBACK_SUSTAINED_TFLOPS = 1400.0
 FALLBACK_HBM_GBS = 6400.0
 KERNEL_SOURCES = ["diffusion_transformer_joint_causal_b300/csrc/dit_attn.cu",
+                  "diffusion_transformer_joint_causal_b300/csrc/fmha_pair.cuh",
                   "diffusion_transformer_joint_causal_b300/csrc/ptx.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fmha_fwd_dram_traffic.txt")
 
@@ -394,6 +396,67 @@ def rmsnorm_roofline(dit, dev, peaks, calls: int = 20):
                          "frac": gbs / peaks["hbm"], "peak_source": f"{peaks['source']} copy"}}
 
 
+def qk8_sweep(dit, dev, peaks, bf16_ms: dict, calls: int = 20):
+    """The e4m3-QK path on the RMS-normalised workloads: the quantising
+    prologue (dit.rmsnorm_e4m3 of Q and of K, out_scale 448/sqrt(d)) and the
+    e4m3-QK forward, each timed with CUDA events over `calls` launches.  S = Q
+    K^T runs at the e4m3 tensor rate (nominally 2x bf16) and P V at the bf16
+    rate, so the contraction's mixed peak is 4/3 of the bf16 one."""
+    import numpy as np
+    import torch
+
+    import workloads as W
+    res = {}
+    for w in W.WORKLOADS:
+        if not w.rms_norm or w.d != 128:
+            continue
+        q, k, v = (torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+                   for x in W.make_qkv(w))
+        inv = float(np.float32(448.0 / math.sqrt(w.d)))
+        s = float(np.float32(math.sqrt(w.d) / 448.0))
+        q8 = torch.empty(q.shape, dtype=torch.float8_e4m3fn, device=dev)
+        k8 = torch.empty(k.shape, dtype=torch.float8_e4m3fn, device=dev)
+        out = torch.empty_like(q)
+
+        def prologue():
+            dit.rmsnorm_e4m3(q, inv, out=q8)
+            dit.rmsnorm_e4m3(k, inv, out=k8)
+
+        def attn():
+            dit.forward_qk8(q8, k8, v, s, s, w.scale, out=out)
+
+        for _ in range(3):
+            prologue()
+            attn()
+        torch.cuda.synchronize(dev)
+        times = {}
+        for name, fn in (("prologue", prologue), ("attention", attn)):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(calls):
+                fn()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            times[name] = e0.elapsed_time(e1) / calls
+        tf = w.flops / times["attention"] / 1e9
+        mixed_peak = peaks["bf16"] * 4.0 / 3.0
+        nbytes = (q.numel() + k.numel()) * 3.0
+        res[w.name] = {
+            "shape": [w.B, w.H, w.Lq, w.Lk, w.d],
+            "ms_attention": times["attention"], "tflops": tf,
+            "speedup_vs_bf16_eager": bf16_ms[w.name] / times["attention"]
+            if w.name in bf16_ms else None,
+            "frac_of_bf16_peak": tf / peaks["bf16"],
+            "frac_of_mixed_peak": tf / mixed_peak,
+            "ms_prologue_q_and_k": times["prologue"],
+            "prologue_gbs": nbytes / (times["prologue"] / 1e3) / 1e9,
+            "prologue_frac_of_hbm": nbytes / (times["prologue"] / 1e3) / 1e9 / peaks["hbm"],
+        }
+        del q, k, v, q8, k8, out
+        torch.cuda.empty_cache()
+    return res
+
+
 def bench_ours(args):
     import numpy as np
     import torch
@@ -508,6 +571,8 @@ def bench_ours(args):
     if world == 1 and not args.no_sweep:
         line["per_workload"] = workload_sweep(dit, dev)
         line["rmsnorm_qk_prologue"] = rmsnorm_roofline(dit, dev, peaks)
+        line["qk8"] = qk8_sweep(dit, dev, peaks,
+                                {n: r["ms_eager"] for n, r in line["per_workload"].items()})
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     print(json.dumps(line), flush=True)

@@ -9,6 +9,12 @@ fallback: if the library is missing, importing the names below raises.
     import diffusion_transformer_joint_causal_b300 as dit
     dit.create()                      # once per device
     out = dit.forward(q, k, v)        # q,k,v: bf16 CUDA tensors [B, H, L, d]
+
+    # e4m3 queries/keys: quantise after the RMS norm, then the e4m3-QK forward
+    s = math.sqrt(128) / 448          # |rms-normalised value| <= sqrt(d)
+    q8 = dit.rmsnorm_e4m3(q, out_scale=1 / s)
+    k8 = dit.rmsnorm_e4m3(k, out_scale=1 / s)
+    out = dit.forward_qk8(q8, k8, v, q_scale=s, k_scale=s)
 """
 from __future__ import annotations
 
@@ -18,7 +24,8 @@ import os
 import threading
 
 __all__ = ["create", "destroy", "forward", "forward_ptr", "status_string", "get_device_error",
-           "check_wait_timeout", "rmsnorm", "rmsnorm_ptr",
+           "check_wait_timeout", "rmsnorm", "rmsnorm_ptr", "forward_qk8", "forward_qk8_ptr",
+           "rmsnorm_e4m3", "rmsnorm_e4m3_ptr",
            "last_cuda_error", "version", "library_path", "DitAttnError", "STATUS",
            "EXPORTED_SYMBOLS"]
 
@@ -32,7 +39,8 @@ STATUS = {
 
 EXPORTED_SYMBOLS = ("dit_attn_version", "dit_attn_create", "dit_attn_forward",
                     "dit_attn_destroy", "dit_attn_status_string", "dit_attn_get_device_error",
-                    "dit_attn_check_wait_timeout", "dit_attn_last_cuda_error", "dit_attn_rmsnorm")
+                    "dit_attn_check_wait_timeout", "dit_attn_last_cuda_error", "dit_attn_rmsnorm",
+                    "dit_attn_forward_qk8", "dit_attn_rmsnorm_e4m3")
 
 _lock = threading.Lock()
 _lib = None
@@ -77,6 +85,12 @@ def _load():
             lib.dit_attn_check_wait_timeout.argtypes = [c_int, vp]
             lib.dit_attn_rmsnorm.restype = c_int
             lib.dit_attn_rmsnorm.argtypes = [vp, vp, vp, ctypes.c_longlong, c_int, ctypes.c_float, vp]
+            lib.dit_attn_forward_qk8.restype = c_int
+            lib.dit_attn_forward_qk8.argtypes = [vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int,
+                                                 ctypes.c_float, ctypes.c_float, ctypes.c_float, vp]
+            lib.dit_attn_rmsnorm_e4m3.restype = c_int
+            lib.dit_attn_rmsnorm_e4m3.argtypes = [vp, vp, vp, ctypes.c_longlong, c_int,
+                                                  ctypes.c_float, ctypes.c_float, vp]
             lib.dit_attn_last_cuda_error.restype = c_int
             lib.dit_attn_last_cuda_error.argtypes = []
             _lib = lib
@@ -134,17 +148,11 @@ def forward_ptr(q: int, k: int, v: int, out: int, B: int, H: int, Lq: int, Lk: i
                                     ctypes.c_float(scale), s)
 
 
-def forward(q, k, v, scale: float | None = None, out=None, stream=None):
-    """out = softmax(q k^T * scale) v over every (batch, head); bf16 in and out.
-
-    q: [B, H, Lq, d], k and v: [B, H, Lk, d], contiguous bf16 CUDA tensors on
-    one device; d is 64 or 128; scale defaults to 1/sqrt(d).  Enqueued on
-    ``stream`` (default: torch's current stream); returns ``out``.
-    """
+def _check_qkv(q, k, v, qk_dtypes):
     import torch
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda:
-            raise TypeError(f"{name} must be a bfloat16 CUDA tensor")
+    for name, t, dtypes in (("q", q, qk_dtypes), ("k", k, qk_dtypes), ("v", v, (torch.bfloat16,))):
+        if not isinstance(t, torch.Tensor) or t.dtype not in dtypes or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA tensor of dtype {' or '.join(map(str, dtypes))}")
         if t.dim() != 4 or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous [B, H, L, d] tensor")
     B, H, Lq, d = q.shape
@@ -153,11 +161,29 @@ def forward(q, k, v, scale: float | None = None, out=None, stream=None):
         raise ValueError("k and v must be [B, H, Lk, d] with q's B, H and d")
     if not (q.device == k.device == v.device):
         raise ValueError("q, k, v must be on one device")
+    return B, H, Lq, Lk, d
+
+
+def _out_like(out, q, shape):
+    import torch
     if out is None:
-        out = torch.empty_like(q)
-    elif (out.dtype != torch.bfloat16 or tuple(out.shape) != tuple(q.shape)
-          or not out.is_contiguous() or out.device != q.device):
+        return torch.empty(shape, dtype=torch.bfloat16, device=q.device)
+    if (out.dtype != torch.bfloat16 or tuple(out.shape) != tuple(shape)
+            or not out.is_contiguous() or out.device != q.device):
         raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    return out
+
+
+def forward(q, k, v, scale: float | None = None, out=None, stream=None):
+    """out = softmax(q k^T * scale) v over every (batch, head); bf16 in and out.
+
+    q: [B, H, Lq, d], k and v: [B, H, Lk, d], contiguous bf16 CUDA tensors on
+    one device; d is 64 or 128; scale defaults to 1/sqrt(d).  Enqueued on
+    ``stream`` (default: torch's current stream); returns ``out``.
+    """
+    import torch
+    B, H, Lq, Lk, d = _check_qkv(q, k, v, (torch.bfloat16,))
+    out = _out_like(out, q, (B, H, Lq, d))
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     with torch.cuda.device(q.device):
@@ -197,4 +223,74 @@ def rmsnorm(x, weight=None, eps: float = 1e-6, out=None, stream=None):
                          x.numel() // d, d, float(eps), _stream_handle(stream))
     if rc:
         raise DitAttnError(rc, "dit_attn_rmsnorm")
+    return out
+
+
+def forward_qk8_ptr(q8: int, k8: int, v: int, out: int, B: int, H: int, Lq: int, Lk: int, d: int,
+                    scale: float, q_scale: float, k_scale: float, stream=0) -> int:
+    """Raw C-ABI call of dit_attn_forward_qk8 with integer device pointers; returns the status."""
+    s = stream if isinstance(stream, ctypes.c_void_p) else ctypes.c_void_p(int(stream))
+    return _load().dit_attn_forward_qk8(ctypes.c_void_p(q8), ctypes.c_void_p(k8),
+                                        ctypes.c_void_p(v), ctypes.c_void_p(out), B, H, Lq, Lk, d,
+                                        ctypes.c_float(scale), ctypes.c_float(q_scale),
+                                        ctypes.c_float(k_scale), s)
+
+
+def forward_qk8(q8, k8, v, q_scale: float, k_scale: float, scale: float | None = None, out=None,
+                stream=None):
+    """out = softmax((q_scale*q8)(k_scale*k8)^T * scale) v with e4m3 q8, k8.
+
+    q8: [B, H, Lq, 128], k8: [B, H, Lk, 128], contiguous CUDA tensors of e4m3
+    codes (torch.float8_e4m3fn or uint8); v: [B, H, Lk, 128] bf16.  scale
+    defaults to 1/sqrt(d).  Returns the bf16 output ``out``.
+    """
+    import torch
+    B, H, Lq, Lk, d = _check_qkv(q8, k8, v, (torch.float8_e4m3fn, torch.uint8))
+    out = _out_like(out, v, (B, H, Lq, d))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    with torch.cuda.device(v.device):
+        rc = forward_qk8_ptr(q8.data_ptr(), k8.data_ptr(), v.data_ptr(), out.data_ptr(),
+                             B, H, Lq, Lk, d, float(scale), float(q_scale), float(k_scale),
+                             _stream_handle(stream))
+    if rc:
+        raise DitAttnError(rc, "dit_attn_forward_qk8")
+    return out
+
+
+def rmsnorm_e4m3_ptr(x: int, y8: int, weight: int, rows: int, d: int, eps: float,
+                     out_scale: float, stream=0) -> int:
+    """Raw C-ABI call of dit_attn_rmsnorm_e4m3 with integer device pointers; returns the status."""
+    s = stream if isinstance(stream, ctypes.c_void_p) else ctypes.c_void_p(int(stream))
+    return _load().dit_attn_rmsnorm_e4m3(ctypes.c_void_p(x), ctypes.c_void_p(y8),
+                                         ctypes.c_void_p(weight) if weight else None,
+                                         ctypes.c_longlong(rows), d, ctypes.c_float(eps),
+                                         ctypes.c_float(out_scale), s)
+
+
+def rmsnorm_e4m3(x, out_scale: float, weight=None, eps: float = 1e-6, out=None, stream=None):
+    """out = e4m3(x / sqrt(mean(x^2, last dim) + eps) * weight * out_scale), saturating at 448,
+    for a bf16 CUDA tensor whose last dimension (64 or 128) is the head dimension.
+    Returns a torch.float8_e4m3fn tensor shaped like x (or fills ``out``)."""
+    import torch
+    if not isinstance(x, torch.Tensor) or x.dtype != torch.bfloat16 or not x.is_cuda:
+        raise TypeError("x must be a bfloat16 CUDA tensor")
+    if not x.is_contiguous() or x.dim() < 1:
+        raise ValueError("x must be contiguous")
+    d = x.shape[-1]
+    if weight is not None and (weight.dtype != torch.bfloat16 or tuple(weight.shape) != (d,)
+                               or not weight.is_contiguous() or weight.device != x.device):
+        raise ValueError("weight must be a contiguous bf16 [d] tensor on x's device")
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.float8_e4m3fn, device=x.device)
+    elif (out.dtype not in (torch.float8_e4m3fn, torch.uint8) or out.shape != x.shape
+          or not out.is_contiguous() or out.device != x.device):
+        raise ValueError("out must be a contiguous e4m3 (or uint8) tensor shaped like x")
+    with torch.cuda.device(x.device):
+        rc = rmsnorm_e4m3_ptr(x.data_ptr(), out.data_ptr(),
+                              weight.data_ptr() if weight is not None else 0,
+                              x.numel() // d, d, float(eps), float(out_scale),
+                              _stream_handle(stream))
+    if rc:
+        raise DitAttnError(rc, "dit_attn_rmsnorm_e4m3")
     return out

@@ -630,7 +630,8 @@ using dit::Traits;
 struct DeviceState {
   bool ready = false;
   int num_sms = 0;
-  int max_pairs = 0;   // co-resident clusters of two CTAs of the pair kernel
+  int max_pairs = 0;       // co-resident clusters of two CTAs of the bf16 pair kernel
+  int max_pairs_qk8 = 0;   // the same for the e4m3-QK pair kernel
 };
 
 constexpr int kMaxDevices = 64;
@@ -652,18 +653,22 @@ bool current_device(int* dev) {
   return *dev >= 0 && *dev < kMaxDevices;
 }
 
-// 3-D bf16 view [BH][L][d] with a 64-column x box_rows box and 128-byte
+// 3-D view [BH][L][d] of bf16 (elem_bytes 2) or e4m3 bytes (elem_bytes 1)
+// with a box of one 128-byte row segment x box_rows rows and 128-byte
 // swizzle.  Rows beyond L inside one head read as zeros, never as the next
 // head's rows.
 int encode_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t L, int d,
-               uint32_t box_rows = 128) {
+               uint32_t box_rows = 128, int elem_bytes = 2) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(L),
                               static_cast<cuuint64_t>(BH)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
-                                 static_cast<cuuint64_t>(L) * static_cast<cuuint64_t>(d) * 2};
-  const cuuint32_t box[3] = {64, box_rows, 1};
+  const cuuint64_t eb = static_cast<cuuint64_t>(elem_bytes);
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * eb,
+                                 static_cast<cuuint64_t>(L) * static_cast<cuuint64_t>(d) * eb};
+  const cuuint32_t box[3] = {128u / static_cast<cuuint32_t>(elem_bytes), box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
+  const CUtensorMapDataType dtype =
+      elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const CUresult r = g_encode(map, dtype, 3, const_cast<void*>(ptr), dims,
                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -717,13 +722,17 @@ cudaLaunchConfig_t pair_launch_config(int grid, cudaStream_t stream, cudaLaunchA
   return cfg;
 }
 
-// d = 128: clusters of two CTAs, one work unit = 512 query rows.
+// d = 128: clusters of two CTAs, one work unit = 512 query rows.  With kQK8,
+// q and k hold e4m3 bytes and `scale` already includes their dequantisation
+// scales.
+template <bool kQK8>
 int launch_pair(const void* q, const void* k, const void* v, void* out, int64_t BH, int Lq, int Lk,
-                float scale, cudaStream_t stream, int max_pairs) {
+                double scale, cudaStream_t stream, int max_pairs) {
   CUtensorMap tq, tk, tv;
   int rc;
-  if ((rc = encode_map(&tq, q, BH, Lq, 128, 128)) != DIT_ATTN_OK) return rc;
-  if ((rc = encode_map(&tk, k, BH, Lk, 128, 64)) != DIT_ATTN_OK) return rc;
+  const int qk_bytes = kQK8 ? 1 : 2;
+  if ((rc = encode_map(&tq, q, BH, Lq, 128, 128, qk_bytes)) != DIT_ATTN_OK) return rc;
+  if ((rc = encode_map(&tk, k, BH, Lk, 128, 64, qk_bytes)) != DIT_ATTN_OK) return rc;
   if ((rc = encode_map(&tv, v, BH, Lk, 128, 128)) != DIT_ATTN_OK) return rc;
   dit::Params p;
   p.out = static_cast<__nv_bfloat16*>(out);
@@ -731,12 +740,58 @@ int launch_pair(const void* q, const void* k, const void* v, void* out, int64_t 
   p.Lk = Lk;
   p.num_qblocks = (Lq + 2 * dit::kUnitRows - 1) / (2 * dit::kUnitRows);
   p.num_units = static_cast<int>(BH * p.num_qblocks);
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.scale_log2 = static_cast<float>(scale * 1.4426950408889634);
   const int pairs = p.num_units < max_pairs ? p.num_units : max_pairs;
   cudaLaunchAttribute attr;
-  cudaLaunchConfig_t cfg = pair_launch_config(2 * pairs, stream, &attr);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, dit::fmha_fwd_pair_kernel, tq, tk, tv, p);
+  cudaLaunchConfig_t cfg =
+      pair_launch_config(2 * pairs, stream, &attr, dit::PairTraitsT<kQK8>::kSmemBytes);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, dit::fmha_fwd_pair_kernel<kQK8>, tq, tk, tv, p);
   if (e != cudaSuccess) return cuda_fail(e);
+  return DIT_ATTN_OK;
+}
+
+// Shared memory and cluster attributes of a pair kernel; *pairs = clusters of
+// two that fit on the device at once.
+template <bool kQK8>
+int setup_pair_kernel(int num_sms, int* pairs) {
+  const uint32_t smem = dit::PairTraitsT<kQK8>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(dit::fmha_fwd_pair_kernel<kQK8>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = cudaFuncSetAttribute(dit::fmha_fwd_pair_kernel<kQK8>,
+                           cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+  if (e != cudaSuccess) return cuda_fail(e);
+  cudaLaunchAttribute attr;
+  cudaLaunchConfig_t cfg = pair_launch_config(num_sms, nullptr, &attr, smem);
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, dit::fmha_fwd_pair_kernel<kQK8>, &cfg);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (clusters < 1) return cuda_fail(cudaErrorInvalidConfiguration);
+  *pairs = clusters;
+  return DIT_ATTN_OK;
+}
+
+// Argument checks shared by the bf16 and e4m3 forwards (qk_bytes = bytes per
+// element of q and k).
+int check_forward_args(const void* q, const void* k, const void* v, const void* out, int B, int H,
+                       int Lq, int Lk, int d, float scale, int qk_bytes) {
+  if (!q || !k || !v || !out) return DIT_ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Lq < 1 || Lk < 1) return DIT_ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || scale < 0.f) return DIT_ATTN_ERR_INVALID_ARG;
+  const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out);
+  if (mis & 15u) return DIT_ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return DIT_ATTN_ERR_UNSUPPORTED;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  const int64_t qblocks = (static_cast<int64_t>(Lq) + dit::kUnitRows - 1) / dit::kUnitRows;
+  if (BH > INT_MAX || Lq > INT_MAX - 2 * dit::kUnitRows || Lk > INT_MAX - 2 * dit::kUnitRows ||
+      BH * qblocks > INT_MAX)
+    return DIT_ATTN_ERR_UNSUPPORTED;
+  const int64_t o_bytes = BH * Lq * d * 2, v_bytes = BH * Lk * d * 2;
+  const int64_t q_bytes = BH * Lq * d * qk_bytes, k_bytes = BH * Lk * d * qk_bytes;
+  if (overlaps(out, o_bytes, q, q_bytes) || overlaps(out, o_bytes, k, k_bytes) ||
+      overlaps(out, o_bytes, v, v_bytes))
+    return DIT_ATTN_ERR_INVALID_ARG;
   return DIT_ATTN_OK;
 }
 
@@ -784,19 +839,14 @@ int dit_attn_create(void) {
   e = cudaFuncSetAttribute(dit::fmha_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Traits<128>::kSmemBytes);
   if (e != cudaSuccess) return cuda_fail(e);
-  e = cudaFuncSetAttribute(dit::fmha_fwd_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           dit::PairTraits::kSmemBytes);
-  if (e != cudaSuccess) return cuda_fail(e);
-  e = cudaFuncSetAttribute(dit::fmha_fwd_pair_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
-  if (e != cudaSuccess) return cuda_fail(e);
   {
-    cudaLaunchAttribute attr;
-    cudaLaunchConfig_t cfg = pair_launch_config(prop.multiProcessorCount, nullptr, &attr);
-    int clusters = 0;
-    e = cudaOccupancyMaxActiveClusters(&clusters, dit::fmha_fwd_pair_kernel, &cfg);
-    if (e != cudaSuccess) return cuda_fail(e);
-    if (clusters < 1) return cuda_fail(cudaErrorInvalidConfiguration);
-    g_state[dev].max_pairs = clusters;
+    int rc = DIT_ATTN_OK, bf16_pairs = 0, qk8_pairs = 0;
+    if ((rc = setup_pair_kernel<false>(prop.multiProcessorCount, &bf16_pairs)) != DIT_ATTN_OK)
+      return rc;
+    if ((rc = setup_pair_kernel<true>(prop.multiProcessorCount, &qk8_pairs)) != DIT_ATTN_OK)
+      return rc;
+    g_state[dev].max_pairs = bf16_pairs;
+    g_state[dev].max_pairs_qk8 = qk8_pairs;
   }
   g_state[dev].num_sms = prop.multiProcessorCount;
   g_state[dev].ready = true;
@@ -813,23 +863,9 @@ int dit_attn_destroy(void) {
 
 int dit_attn_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int Lq,
                      int Lk, int d, float scale, void* stream) {
-  if (!q || !k || !v || !out) return DIT_ATTN_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || Lq < 1 || Lk < 1) return DIT_ATTN_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || scale < 0.f) return DIT_ATTN_ERR_INVALID_ARG;
-  const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out);
-  if (mis & 15u) return DIT_ATTN_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return DIT_ATTN_ERR_UNSUPPORTED;
+  const int rc = check_forward_args(q, k, v, out, B, H, Lq, Lk, d, scale, 2);
+  if (rc != DIT_ATTN_OK) return rc;
   const int64_t BH = static_cast<int64_t>(B) * H;
-  const int64_t qblocks = (static_cast<int64_t>(Lq) + dit::kUnitRows - 1) / dit::kUnitRows;
-  if (BH > INT_MAX || Lq > INT_MAX - 2 * dit::kUnitRows || Lk > INT_MAX - 2 * dit::kUnitRows ||
-      BH * qblocks > INT_MAX)
-    return DIT_ATTN_ERR_UNSUPPORTED;
-  const int64_t q_bytes = BH * Lq * d * 2, kv_bytes = BH * Lk * d * 2;
-  if (overlaps(out, q_bytes, q, q_bytes) || overlaps(out, q_bytes, k, kv_bytes) ||
-      overlaps(out, q_bytes, v, kv_bytes))
-    return DIT_ATTN_ERR_INVALID_ARG;
-
   int dev = -1;
   if (!current_device(&dev)) return DIT_ATTN_ERR_NO_DEVICE;
   int num_sms, max_pairs;
@@ -841,7 +877,30 @@ int dit_attn_forward(const void* q, const void* k, const void* v, void* out, int
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return d == 64 ? launch<64>(q, k, v, out, BH, Lq, Lk, scale, s, num_sms)
-                 : launch_pair(q, k, v, out, BH, Lq, Lk, scale, s, max_pairs);
+                 : launch_pair<false>(q, k, v, out, BH, Lq, Lk, scale, s, max_pairs);
+}
+
+int dit_attn_forward_qk8(const void* q8, const void* k8, const void* v, void* out, int B, int H,
+                         int Lq, int Lk, int d, float scale, float q_scale, float k_scale,
+                         void* stream) {
+  int rc = check_forward_args(q8, k8, v, out, B, H, Lq, Lk, d, scale, 1);
+  if (rc != DIT_ATTN_OK) return rc;
+  if (!std::isfinite(q_scale) || !std::isfinite(k_scale) || q_scale < 0.f || k_scale < 0.f)
+    return DIT_ATTN_ERR_INVALID_ARG;
+  const double logit_scale = static_cast<double>(scale) * q_scale * k_scale;
+  if (!(logit_scale <= 3.0e38)) return DIT_ATTN_ERR_INVALID_ARG;
+  if (d != 128) return DIT_ATTN_ERR_UNSUPPORTED;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  int dev = -1;
+  if (!current_device(&dev)) return DIT_ATTN_ERR_NO_DEVICE;
+  int max_pairs;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_state[dev].ready) return DIT_ATTN_ERR_NOT_INITIALIZED;
+    max_pairs = g_state[dev].max_pairs_qk8;
+  }
+  return launch_pair<true>(q8, k8, v, out, BH, Lq, Lk, logit_scale,
+                           static_cast<cudaStream_t>(stream), max_pairs);
 }
 
 int dit_attn_check_wait_timeout(int limit_us, void* stream) {
@@ -859,18 +918,25 @@ int dit_attn_check_wait_timeout(int limit_us, void* stream) {
   return DIT_ATTN_OK;
 }
 
-int dit_attn_rmsnorm(const void* x, void* y, const void* weight, long long rows, int d, float eps,
-                     void* stream) {
+}  // extern "C"
+
+namespace {
+
+// y_bytes = bytes per output element: 2 (bf16, y may equal x) or 1 (e4m3).
+int rmsnorm_impl(const void* x, void* y, const void* weight, long long rows, int d, float eps,
+                 float out_scale, int y_bytes, void* stream) {
   if (!x || !y) return DIT_ATTN_ERR_INVALID_ARG;
   if (rows < 1 || !std::isfinite(eps) || eps < 0.f) return DIT_ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(out_scale) || out_scale <= 0.f) return DIT_ATTN_ERR_INVALID_ARG;
   const uintptr_t mis = reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y) |
                         reinterpret_cast<uintptr_t>(weight);
   if (mis & 15u) return DIT_ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return DIT_ATTN_ERR_UNSUPPORTED;
   if (rows > (static_cast<long long>(1) << 40)) return DIT_ATTN_ERR_UNSUPPORTED;
-  const int64_t bytes = static_cast<int64_t>(rows) * d * 2;
-  if (x != y && overlaps(x, bytes, y, bytes)) return DIT_ATTN_ERR_INVALID_ARG;
-  if (weight && (overlaps(weight, d * 2, y, bytes))) return DIT_ATTN_ERR_INVALID_ARG;
+  const int64_t x_bytes = static_cast<int64_t>(rows) * d * 2;
+  const int64_t out_bytes = static_cast<int64_t>(rows) * d * y_bytes;
+  if (!(y_bytes == 2 && x == y) && overlaps(x, x_bytes, y, out_bytes)) return DIT_ATTN_ERR_INVALID_ARG;
+  if (weight && (overlaps(weight, d * 2, y, out_bytes))) return DIT_ATTN_ERR_INVALID_ARG;
   int dev = -1;
   if (!current_device(&dev)) return DIT_ATTN_ERR_NO_DEVICE;
   int num_sms;
@@ -885,13 +951,31 @@ int dit_attn_rmsnorm(const void* x, void* y, const void* weight, long long rows,
   const int grid = static_cast<int>(want < cap ? want : cap);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const uint4* xv = static_cast<const uint4*>(x);
-  uint4* yv = static_cast<uint4*>(y);
   const uint4* wv = static_cast<const uint4*>(weight);
-  if (d == 64) dit::rmsnorm_kernel<64><<<grid, 256, 0, s>>>(xv, yv, wv, rows, eps);
-  else dit::rmsnorm_kernel<128><<<grid, 256, 0, s>>>(xv, yv, wv, rows, eps);
+  if (y_bytes == 2) {
+    if (d == 64) dit::rmsnorm_kernel<64, false><<<grid, 256, 0, s>>>(xv, y, wv, rows, eps, 1.f);
+    else dit::rmsnorm_kernel<128, false><<<grid, 256, 0, s>>>(xv, y, wv, rows, eps, 1.f);
+  } else {
+    if (d == 64) dit::rmsnorm_kernel<64, true><<<grid, 256, 0, s>>>(xv, y, wv, rows, eps, out_scale);
+    else dit::rmsnorm_kernel<128, true><<<grid, 256, 0, s>>>(xv, y, wv, rows, eps, out_scale);
+  }
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   return DIT_ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dit_attn_rmsnorm(const void* x, void* y, const void* weight, long long rows, int d, float eps,
+                     void* stream) {
+  return rmsnorm_impl(x, y, weight, rows, d, eps, 1.f, 2, stream);
+}
+
+int dit_attn_rmsnorm_e4m3(const void* x, void* y8, const void* weight, long long rows, int d,
+                          float eps, float out_scale, void* stream) {
+  return rmsnorm_impl(x, y8, weight, rows, d, eps, out_scale, 1, stream);
 }
 
 int dit_attn_get_device_error(void* stream) {

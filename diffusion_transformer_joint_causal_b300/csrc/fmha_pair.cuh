@@ -16,18 +16,28 @@
 // (the leader's producer posts the byte count of both halves); MMA completion
 // is multicast to the barriers of both CTAs; each softmax warp reports P-ready
 // on the leader's barrier.  Every wait is bounded like the single-CTA kernel's.
+//
+// kQK8 selects e4m3 queries and keys: S = Q K^T runs as kind::f8f6f4 MMAs (32
+// bytes of K per instruction, half the tensor time of bf16 for the same
+// product), with the per-tensor dequantisation scales folded into the softmax
+// scale.  P and V stay bf16, so the second product and the softmax are
+// unchanged.  A query tile and a key half are one 128-byte-wide box each; the
+// shared memory this frees over bf16 holds two more pipeline stages.
 #pragma once
 
 namespace dit {
 
-struct PairTraits {
+template <bool kQK8>
+struct PairTraitsT {
   static constexpr int D = 128;
-  static constexpr int kBoxCols = 64;
+  static constexpr int kBoxCols = 64;                       // bf16 columns in a 128-byte box row
+  static constexpr int kQKBoxes = kQK8 ? 1 : 2;             // 128-byte boxes across d for Q, K
   static constexpr uint32_t kQBoxBytes = 128u * 128u;       // 128 rows x 128 bytes
-  static constexpr uint32_t kQTileBytes = 2 * kQBoxBytes;   // one 128 x 128 query tile
-  static constexpr uint32_t kKBoxBytes = 64u * 128u;        // 64 keys x 64 columns
-  static constexpr uint32_t kHalfBytes = 16384;             // one K half or V half
-  static constexpr int kStages = 8;
+  static constexpr uint32_t kQTileBytes = kQKBoxes * kQBoxBytes;   // one 128-row query tile
+  static constexpr uint32_t kKBoxBytes = 64u * 128u;        // 64 keys x 128 bytes
+  static constexpr uint32_t kKHalfBytes = kQKBoxes * kKBoxBytes;   // one K half
+  static constexpr uint32_t kHalfBytes = 16384;             // a stage: one V half (or K half)
+  static constexpr int kStages = kQK8 ? 10 : 8;
   __host__ __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
   __host__ __device__ static constexpr uint32_t col_o(int t) { return 256u + 128u * t; }
   static constexpr uint32_t kTmemCols = 512;
@@ -47,11 +57,13 @@ struct PairTraits {
   static constexpr uint32_t kSmemBytes = 1024 + kOffMisc + 16;
   static constexpr uint32_t kPFullArrivals = 16;     // 8 softmax warps x 2 CTAs
 };
+using PairTraits = PairTraitsT<false>;
 
 // ----------------------------------------------------------------- producer (both CTAs)
+template <bool kQK8>
 __device__ void pair_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                const CUtensorMap* tmV, const Params& p, const Shared& sh) {
-  using T = PairTraits;
+  using T = PairTraitsT<kQK8>;
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
   const uint64_t pol_kv = policy_evict_last();
@@ -66,16 +78,16 @@ __device__ void pair_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
     if (!mbar_wait(sh.bar(T::kBarQEmpty + t), (it & 1u) ^ 1u, kWaitLimitNs, sh.abort)) return false;
     if (leader) mbar_arrive_expect_tx(sh.bar(T::kBarQFull + t), 2 * T::kQTileBytes);
     const uint32_t dst = sh.base + T::kOffQ + t * T::kQTileBytes;
-    for (int b = 0; b < 2; ++b)
+    for (int b = 0; b < T::kQKBoxes; ++b)
       tma_load_3d_pair(dst + b * T::kQBoxBytes, tmQ, qfull0_leader + 8u * t, b * T::kBoxCols,
                        row0 + t * kBM, bh, pol_q);
     q_fills |= 1u << t;
     q_parity = (q_parity & ~(1u << t)) | ((it & 1u) << t);
     return true;
   };
-  auto take_empty = [&]() -> bool {
+  auto take_empty = [&](uint32_t half_bytes) -> bool {
     if (!mbar_wait(sh.bar(T::kBarEmpty + stage), phase ^ 1u, kWaitLimitNs, sh.abort)) return false;
-    if (leader) mbar_arrive_expect_tx(sh.bar(T::kBarFull + stage), 2 * T::kHalfBytes);
+    if (leader) mbar_arrive_expect_tx(sh.bar(T::kBarFull + stage), 2 * half_bytes);
     return true;
   };
   auto advance = [&]() {
@@ -89,12 +101,12 @@ __device__ void pair_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
     const int row0 = (u % p.num_qblocks) * (2 * kUnitRows) + static_cast<int>(rank) * kUnitRows;
     ok = load_q(0, bh, row0);
     for (int j = 0; j < n_kv && ok; ++j) {
-      // K half: keys j*128 + 64*rank .. +63, all 128 columns (two 64-column boxes)
-      ok = take_empty();
+      // K half: keys j*128 + 64*rank .. +63, all d columns (128-byte boxes)
+      ok = take_empty(T::kKHalfBytes);
       if (!ok) break;
       {
         const uint32_t dst = sh.base + T::kOffKV + stage * T::kHalfBytes;
-        for (int b = 0; b < 2; ++b)
+        for (int b = 0; b < T::kQKBoxes; ++b)
           tma_load_3d_pair(dst + b * T::kKBoxBytes, tmK, full0_leader + 8u * stage, b * T::kBoxCols,
                            j * kBN + static_cast<int>(rank) * 64, bh, pol_kv);
       }
@@ -104,7 +116,7 @@ __device__ void pair_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
         if (!ok) break;
       }
       // V half: keys j*128 .. +127, columns 64*rank .. +63
-      ok = take_empty();
+      ok = take_empty(T::kHalfBytes);
       if (!ok) break;
       tma_load_3d_pair(sh.base + T::kOffKV + stage * T::kHalfBytes, tmV, full0_leader + 8u * stage,
                        static_cast<int>(rank) * T::kBoxCols, j * kBN, bh, pol_kv);
@@ -136,15 +148,25 @@ __device__ void pair_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
 }
 
 // ----------------------------------------------------------------- MMA issuer (leader CTA)
+template <bool kQK8>
 __device__ __forceinline__ void pair_issue_qk(uint32_t d_tmem, uint32_t q_lo, uint32_t k_lo) {
-  using T = PairTraits;
-  constexpr uint32_t idesc = idesc_bf16_f32(2 * kBM, kBN, 0, 0);
+  using T = PairTraitsT<kQK8>;
   constexpr uint32_t hi = desc_hi_sw128(1024);
+  if constexpr (kQK8) {
+    // one 128-byte box row holds all of d; each instruction takes 32 bytes of it
+    constexpr uint32_t idesc = idesc_e4m3_f32(2 * kBM, kBN);
 #pragma unroll
-  for (int k = 0; k < T::D / 16; ++k) {
-    const uint32_t a_off = ((k / 4) * T::kQBoxBytes + (k % 4) * 32) >> 4;
-    const uint32_t b_off = ((k / 4) * T::kKBoxBytes + (k % 4) * 32) >> 4;
-    mma_ss_lo_pair(d_tmem, q_lo + a_off, k_lo + b_off, hi, idesc, k > 0 ? 1u : 0u);
+    for (int k = 0; k < T::D / 32; ++k)
+      mma_ss_lo_pair_f8(d_tmem, q_lo + ((k * 32) >> 4), k_lo + ((k * 32) >> 4), hi, idesc,
+                        k > 0 ? 1u : 0u);
+  } else {
+    constexpr uint32_t idesc = idesc_bf16_f32(2 * kBM, kBN, 0, 0);
+#pragma unroll
+    for (int k = 0; k < T::D / 16; ++k) {
+      const uint32_t a_off = ((k / 4) * T::kQBoxBytes + (k % 4) * 32) >> 4;
+      const uint32_t b_off = ((k / 4) * T::kKBoxBytes + (k % 4) * 32) >> 4;
+      mma_ss_lo_pair(d_tmem, q_lo + a_off, k_lo + b_off, hi, idesc, k > 0 ? 1u : 0u);
+    }
   }
 }
 
@@ -158,8 +180,9 @@ __device__ __forceinline__ void pair_issue_pv(uint32_t d_tmem, uint32_t p_tmem, 
                    idesc, (accumulate || k > 0) ? 1u : 0u);
 }
 
+template <bool kQK8>
 __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) {
-  using T = PairTraits;
+  using T = PairTraitsT<kQK8>;
   constexpr uint16_t kBoth = 3;
   const bool issuer = (threadIdx.x & 31) == 0;
   uint32_t stage = 0, phase = 0, g = 0, it = 0;
@@ -191,7 +214,7 @@ __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) 
     if (!ok) break;
     tc_fence_after();
     if (issuer) {
-      pair_issue_qk(tmem + T::col_s(0), q_lo0, kv_lo(sK));
+      pair_issue_qk<kQK8>(tmem + T::col_s(0), q_lo0, kv_lo(sK));
       mma_commit_pair(sh.bar(T::kBarSFull + 0), kBoth);
       if (n_kv == 1) mma_commit_pair(sh.bar(T::kBarQEmpty + 0), kBoth);
     }
@@ -200,7 +223,7 @@ __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) 
     if (!ok) break;
     tc_fence_after();
     if (issuer) {
-      pair_issue_qk(tmem + T::col_s(1), q_lo1, kv_lo(sK));
+      pair_issue_qk<kQK8>(tmem + T::col_s(1), q_lo1, kv_lo(sK));
       mma_commit_pair(sh.bar(T::kBarSFull + 1), kBoth);
       if (n_kv == 1) mma_commit_pair(sh.bar(T::kBarQEmpty + 1), kBoth);
       mma_commit_pair(sh.bar(T::kBarEmpty + sK), kBoth);
@@ -216,7 +239,7 @@ __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) 
       if (issuer) {
         pair_issue_pv(tmem + T::col_o(0), tmem + T::col_s(0), kv_lo(sV), j > 0);
         if (more) {
-          pair_issue_qk(tmem + T::col_s(0), q_lo0, kv_lo(sK_next));
+          pair_issue_qk<kQK8>(tmem + T::col_s(0), q_lo0, kv_lo(sK_next));
           mma_commit_pair(sh.bar(T::kBarSFull + 0), kBoth);
           if (j + 2 == n_kv) mma_commit_pair(sh.bar(T::kBarQEmpty + 0), kBoth);
         } else {
@@ -231,7 +254,7 @@ __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) 
       if (issuer) {
         pair_issue_pv(tmem + T::col_o(1), tmem + T::col_s(1), kv_lo(sV), j > 0);
         if (more) {
-          pair_issue_qk(tmem + T::col_s(1), q_lo1, kv_lo(sK_next));
+          pair_issue_qk<kQK8>(tmem + T::col_s(1), q_lo1, kv_lo(sK_next));
           mma_commit_pair(sh.bar(T::kBarEmpty + sV), kBoth);
           mma_commit_pair(sh.bar(T::kBarSFull + 1), kBoth);
           if (j + 2 == n_kv) mma_commit_pair(sh.bar(T::kBarQEmpty + 1), kBoth);
@@ -257,11 +280,12 @@ __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) 
 
 // ----------------------------------------------------------------- kernel
 // Launched with a cluster dimension of 2 (consecutive CTAs form a pair).
+template <bool kQK8>
 __global__ void __launch_bounds__(kNumThreads, 1)
     fmha_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const Params p) {
-  using T = PairTraits;
+  using T = PairTraitsT<kQK8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -312,10 +336,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     softmax_role<T::D, T, true>(p, sh, tmem);
   } else if (warp == kMmaWarp) {
     reg_dealloc<kRegsOther>();
-    if (leader) pair_mma_role(p, sh, tmem);
+    if (leader) pair_mma_role<kQK8>(p, sh, tmem);
   } else if (warp == kLoadWarp) {
     reg_dealloc<kRegsOther>();
-    if (lane == 0) pair_load_role(&tmQ, &tmK, &tmV, p, sh);
+    if (lane == 0) pair_load_role<kQK8>(&tmQ, &tmK, &tmV, p, sh);
     __syncwarp();
   } else {
     reg_dealloc<kRegsOther>();

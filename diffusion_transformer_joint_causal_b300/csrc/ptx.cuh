@@ -387,6 +387,18 @@ __device__ __forceinline__ void mma_ss_lo_pair(uint32_t d_tmem, uint32_t a_lo, u
       "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// S = Q K^T with e4m3 operands (K = 32 bytes per instruction).
+__device__ __forceinline__ void mma_ss_lo_pair_f8(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                                  uint32_t hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 da, {%1, %3};\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], da, db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 __device__ __forceinline__ void mma_ts_lo_pair(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
                                                uint32_t hi, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -452,6 +464,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
          | (1u << 10)                               // B format: bf16
          | (static_cast<uint32_t>(a_mn) << 15)      // A major
          | (static_cast<uint32_t>(b_mn) << 16)      // B major
+         | (static_cast<uint32_t>(N >> 3) << 17)    // N
+         | (static_cast<uint32_t>(M >> 4) << 24);   // M
+}
+
+// Instruction descriptor for kind::f8f6f4 with e4m3 A/B (format code 0, both
+// K-major) and an fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4)                                  // D format: f32
          | (static_cast<uint32_t>(N >> 3) << 17)    // N
          | (static_cast<uint32_t>(M >> 4) << 24);   // M
 }

@@ -1,19 +1,28 @@
 // RMS normalisation of queries or keys, per token and head, over the head
 // dimension: y[r, :] = bf16(x[r, :] / sqrt(mean(x[r, :]^2) + eps) * w), with
 // fp32 arithmetic.  The normalised workloads of the joint attention apply it
-// to Q and K before the attention forward.
+// to Q and K before the attention forward.  With kE4M3 the same value times
+// out_scale is rounded to e4m3 (nearest even, saturating at +-448) instead:
+// the quantising prologue of the e4m3-QK forward, one pass over the tensor.
 //
-// HBM-bound: every row is read once and written once.  A lane moves 16 bytes
+// HBM-bound: every row is read once and written once.  A lane reads 16 bytes
 // (8 bf16) per access; D/8 lanes cover a row, so one warp instruction reads
 // 512 contiguous bytes; each lane group keeps kRowsInFlight rows in flight.
 #pragma once
 
 namespace dit {
 
-template <int D>
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  uint16_t lo, hi;   // the first operand of the conversion lands in the upper byte
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+template <int D, bool kE4M3>
 __global__ void __launch_bounds__(256)
-    rmsnorm_kernel(const uint4* x, uint4* y, const uint4* __restrict__ w,
-                   int64_t rows, float eps) {
+    rmsnorm_kernel(const uint4* x, void* y, const uint4* __restrict__ w, int64_t rows, float eps,
+                   float out_scale) {
   constexpr int kLanesPerRow = D / 8;
   constexpr int kRowsPerWarp = 32 / kLanesPerRow;
   constexpr int kRowsInFlight = 4;
@@ -61,12 +70,21 @@ __global__ void __launch_bounds__(256)
       for (int off = kLanesPerRow / 2; off > 0; off /= 2)
         ss += __shfl_xor_sync(0xffffffffu, ss, off);
       const float inv = rsqrtf(ss * (1.f / D) + eps);
-      uint32_t o[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        o[i] = pack_bf16x2(f[2 * i] * inv * wf[2 * i], f[2 * i + 1] * inv * wf[2 * i + 1]);
       const int64_t r = base + u * kRowsPerWarp + grp;
-      if (r < rows) y[r * kLanesPerRow + chunk] = make_uint4(o[0], o[1], o[2], o[3]);
+      if constexpr (kE4M3) {
+        float g[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) g[i] = f[i] * inv * wf[i] * out_scale;
+        const uint2 o = make_uint2(pack_e4m3x4(g[0], g[1], g[2], g[3]),
+                                   pack_e4m3x4(g[4], g[5], g[6], g[7]));
+        if (r < rows) static_cast<uint2*>(y)[r * kLanesPerRow + chunk] = o;
+      } else {
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          o[i] = pack_bf16x2(f[2 * i] * inv * wf[2 * i], f[2 * i + 1] * inv * wf[2 * i + 1]);
+        if (r < rows) static_cast<uint4*>(y)[r * kLanesPerRow + chunk] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
     }
   }
 }

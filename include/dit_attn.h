@@ -76,6 +76,34 @@ int dit_attn_forward(const void* q, const void* k, const void* v, void* out, int
                      int Lk, int d, float scale, void* stream);
 
 /*
+ * The same attention with e4m3 queries and keys ("cuDNN FP8 attention" is the
+ * FP8 attention that "Speed Up Image Generation with FLUX 3 Image Klein on
+ * NVIDIA Blackwell GPUs" (Key takeaways, fourth item) and the sns.style
+ * article on TensorRT LLM VisualGen and FLUX 3 Image Klein (third paragraph)
+ * compare against dense BF16 attention; the pages print no FP8 recipe):
+ *
+ *     s_ij = scale * q_scale * k_scale * sum_c e4m3(q8[b,h,i,c]) * e4m3(k8[b,h,j,c])
+ *     o[b,h,i,:] = sum_j softmax_j(s_ij) * v[b,h,j,:]
+ *
+ * q8 : device pointer, e4m3 codes (1 byte; OCP FP8 E4M3, bias 7, no
+ *      infinities), contiguous [B, H, Lq, d], dequantised value = code value
+ *      * q_scale
+ * k8 : the same for keys, [B, H, Lk, d], with k_scale
+ * v, out: bf16, as in dit_attn_forward.
+ * d must be 128 (else UNSUPPORTED).  q_scale, k_scale finite and >= 0, and
+ * scale*q_scale*k_scale at most 3e38 (else INVALID_ARG); the product is
+ * folded into the softmax scale once.  Arithmetic: e4m3 tensor-core products
+ * with exact fp32 accumulation for S; the softmax, P (bf16), P.V and the
+ * output as in dit_attn_forward.  Sizes, alignment, overlap, stream and error
+ * behaviour as in dit_attn_forward (q8, k8 sizes counted in bytes).
+ * The NaN codes 0x7F and 0xFF are not valid inputs; rows that meet them
+ * have unspecified values.
+ */
+int dit_attn_forward_qk8(const void* q8, const void* k8, const void* v, void* out, int B, int H,
+                         int Lq, int Lk, int d, float scale, float q_scale, float k_scale,
+                         void* stream);
+
+/*
  * RMS normalisation of queries or keys over the head dimension, per token and
  * head (the normalisation the 1024x1024 and 2048x2048 workloads apply to Q
  * and K before attention; the pages do not print it, so no weight is implied):
@@ -90,6 +118,22 @@ int dit_attn_forward(const void* q, const void* k, const void* v, void* out, int
  */
 int dit_attn_rmsnorm(const void* x, void* y, const void* weight, long long rows, int d, float eps,
                      void* stream);
+
+/*
+ * The quantising prologue of dit_attn_forward_qk8: RMS normalisation as in
+ * dit_attn_rmsnorm, multiplied by out_scale (the reciprocal of the tensor's
+ * dequantisation scale) and rounded to e4m3, all in fp32:
+ *
+ *     y8[r, c] = e4m3( x[r, c] / sqrt(mean_c' x[r, c']^2 + eps) * weight[c] * out_scale )
+ *
+ * e4m3(): round to nearest, ties to even; magnitudes beyond 448 saturate to
+ * +-448.  With eps = 0 and no weight every |value| is at most sqrt(d), so
+ * out_scale = 448 / sqrt(d) never saturates.  x: device bf16 [rows, d];
+ * y8: device [rows, d] bytes, must not overlap x or weight; weight as in
+ * dit_attn_rmsnorm.  out_scale finite and > 0.  Otherwise as dit_attn_rmsnorm.
+ */
+int dit_attn_rmsnorm_e4m3(const void* x, void* y8, const void* weight, long long rows, int d,
+                          float eps, float out_scale, void* stream);
 
 /* Forget the current device's state; forward then returns NOT_INITIALIZED. */
 int dit_attn_destroy(void);

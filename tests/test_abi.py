@@ -123,3 +123,68 @@ def test_rmsnorm_rejects_bad_arguments(args, expect):
 @pytest.mark.skipif(_has_gpu(), reason="checks the no-device path")
 def test_rmsnorm_no_device():
     assert dit.rmsnorm_ptr(A, A, 0, 8, 128, 1e-6) == 4      # in place is allowed
+
+
+QK8 = (A, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 8, 8, 128, 0.125, 0.02, 0.03)
+
+
+def _qk8(**change):
+    names = ("q8", "k8", "v", "out", "B", "H", "Lq", "Lk", "d", "scale", "q_scale", "k_scale")
+    args = dict(zip(names, QK8))
+    args.update(change)
+    return tuple(args[n] for n in names)
+
+
+@pytest.mark.parametrize("args,expect", [
+    (_qk8(q8=0), 1),                                  # null q8
+    (_qk8(v=0), 1),                                   # null v
+    (_qk8(Lk=0), 1),                                  # Lk = 0
+    (_qk8(k8=A + MB + 8), 1),                         # misaligned k8
+    (_qk8(q_scale=float("nan")), 1),                  # NaN q_scale
+    (_qk8(k_scale=-1.0), 1),                          # negative k_scale
+    (_qk8(k_scale=float("inf")), 1),                  # inf k_scale
+    (_qk8(scale=1e20, q_scale=1e20, k_scale=1e20), 1),  # combined scale overflows fp32
+    (_qk8(out=A + 512), 1),                           # out overlaps the 1 KB of q8
+    (_qk8(d=64), 2),                                  # e4m3 path is d = 128 only
+    (_qk8(d=96), 2),
+    (_qk8(B=65536, H=65536), 2),                      # B*H too large
+])
+def test_forward_qk8_rejects_bad_arguments(args, expect):
+    assert dit.forward_qk8_ptr(*args) == expect
+
+
+@pytest.mark.skipif(_has_gpu(), reason="a valid call with fake pointers must not reach a GPU")
+def test_forward_qk8_overlap_counts_e4m3_bytes():
+    # q8 is 8*128 = 1 KB of e4m3 codes: an out placed right after it does not
+    # overlap (a bf16-sized count would say it does), so the call passes every
+    # argument check and stops at the device check.
+    assert dit.forward_qk8_ptr(*_qk8(out=A + 1024)) == 4
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((0, A + MB, 0, 8, 128, 1e-6, 1.0), 1),           # null x
+    ((A, A + MB, 0, 8, 128, 1e-6, 0.0), 1),           # zero out_scale
+    ((A, A + MB, 0, 8, 128, 1e-6, float("inf")), 1),  # inf out_scale
+    ((A, A + MB, 0, 8, 128, -1.0, 1.0), 1),           # negative eps
+    ((A, A + 8, 0, 8, 128, 1e-6, 1.0), 1),            # misaligned y8
+    ((A, A, 0, 8, 128, 1e-6, 1.0), 1),                # in place is not allowed for e4m3
+    ((A, A + 1024, 0, 8, 128, 1e-6, 1.0), 1),         # y8 overlaps x (2 KB of bf16)
+    ((A, A + MB, 0, 8, 96, 1e-6, 1.0), 2),            # d = 96
+])
+def test_rmsnorm_e4m3_rejects_bad_arguments(args, expect):
+    assert dit.rmsnorm_e4m3_ptr(*args) == expect
+
+
+@pytest.mark.skipif(_has_gpu(), reason="checks the no-device path")
+def test_e4m3_entry_points_no_device():
+    assert dit.forward_qk8_ptr(*QK8) == 4
+    assert dit.rmsnorm_e4m3_ptr(A, A + 2048, 0, 8, 128, 1e-6, 1.0) == 4   # y8 right after x
+
+
+def test_python_e4m3_wrappers_check_tensors():
+    import torch
+    x = torch.zeros(1, 1, 8, 128, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        dit.forward_qk8(x, x, x, 1.0, 1.0)                # bf16 q8 / CPU tensors
+    with pytest.raises(TypeError):
+        dit.rmsnorm_e4m3(x, 1.0)                          # CPU tensor

@@ -80,3 +80,41 @@ def test_sample_rows():
     assert np.array_equal(r, W.sample_rows(w, 0, 5))
     assert not np.array_equal(r, W.sample_rows(w, 0, 6))
     assert np.array_equal(W.sample_rows(W.workload("tiny"), 0, 1), np.arange(256))
+
+
+def test_e4m3_round_to_nearest_even_matches_torch():
+    rng = np.random.default_rng(3)
+    x = np.concatenate([
+        rng.standard_normal(200000).astype(np.float32) * np.float32(40.0),
+        rng.standard_normal(20000).astype(np.float32) * np.float32(0.01),     # subnormal range
+        np.array([0.0, 448.0, 449.0, 1000.0, -1000.0, 2.0 ** -9, 2.0 ** -10, 3 * 2.0 ** -11,
+                  1.0625, 1.1875, 240.0, 248.0, 232.0], np.float32),
+    ])
+    ours = W.e4m3_bits(x)
+    xt = torch.from_numpy(np.clip(x, -448, 448))          # torch saturates only via clamp
+    ref = xt.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+    back = torch.from_numpy(ours.copy()).view(torch.float8_e4m3fn).float().numpy()
+    assert np.array_equal(W.e4m3_to_f32(ours), back)
+
+
+def test_quantize_e4m3_per_tensor_scale():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((3, 50)).astype(np.float32) * np.float32(7.0)
+    codes, scale = W.quantize_e4m3(x)
+    deq = W.e4m3_to_f32(codes) * scale
+    assert np.abs(deq).max() <= 448 * scale * (1 + 1e-6)
+    np.testing.assert_allclose(deq, x, rtol=2 ** -3, atol=scale * 2.0 ** -9)
+
+
+def test_e4m3_every_value_and_midpoint():
+    # every non-negative finite e4m3 value, and float32 neighbours of every
+    # midpoint between consecutive values (ties go to the even code)
+    vals = W.e4m3_to_f32(np.arange(0x7F, dtype=np.uint8))
+    assert np.array_equal(W.e4m3_bits(vals), np.arange(0x7F, dtype=np.uint8))
+    mids = ((vals[:-1].astype(np.float64) + vals[1:]) / 2).astype(np.float32)
+    x = np.concatenate([mids, np.nextafter(mids, np.float32(0)), np.nextafter(mids, np.float32(1e9))])
+    x = np.concatenate([x, -x])
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(W.e4m3_bits(x), ref)
+    assert vals[0x7E] == 448.0 and vals[1] == 2.0 ** -9 and vals[8] == 2.0 ** -6

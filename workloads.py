@@ -33,7 +33,8 @@ import numpy as np
 
 __all__ = [
     "Workload", "WORKLOADS", "workload", "bf16_bits", "bf16_to_f32",
-    "make_qkv", "sample_rows", "attention_flops",
+    "make_qkv", "sample_rows", "attention_flops", "e4m3_bits", "e4m3_to_f32",
+    "quantize_e4m3",
 ]
 
 
@@ -103,6 +104,46 @@ def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
     """Widen bfloat16 bit patterns to float32 (exact)."""
     b = np.ascontiguousarray(bits, dtype=np.uint16)
     return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def _e4m3_table() -> np.ndarray:
+    """Values of the 127 non-negative finite e4m3 codes 0x00..0x7E (bias 7, no inf)."""
+    codes = np.arange(0x7F, dtype=np.int64)
+    e, m = codes >> 3, codes & 7
+    return np.where(e == 0, np.ldexp(m / 8.0, -6), np.ldexp(1.0 + m / 8.0, e - 7))
+
+
+_E4M3 = _e4m3_table()
+
+
+def e4m3_to_f32(codes: np.ndarray) -> np.ndarray:
+    """Widen e4m3 codes (uint8; 0x7F/0xFF NaN are not produced here) to float32."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8).astype(np.int64)
+    mag = _E4M3[np.minimum(c & 0x7F, 0x7E)]
+    return np.where(c & 0x80, -mag, mag).astype(np.float32)
+
+
+def e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to e4m3 (nearest, ties to even; saturate at 448; sign kept on zero)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if not np.all(np.isfinite(x)):
+        raise ValueError("non-finite input")
+    a = np.minimum(np.abs(x), np.float32(448.0))
+    u = a.view(np.uint32)
+    # normal binades: keep 3 of float32's 23 mantissa bits (ties to even), rebias 127 -> 7
+    normal = ((u + np.uint32(0x7FFFF) + ((u >> np.uint32(20)) & np.uint32(1))) >> np.uint32(20)) \
+        - np.uint32((127 - 7) << 3)
+    # below 2^-6 the spacing is 2^-9 and the code is the multiple of it
+    sub = np.rint(a * np.float32(512.0)).astype(np.uint32)
+    code = np.where(a < np.float32(2.0 ** -6), sub, normal).astype(np.uint8)
+    return np.where(np.signbit(x), code | np.uint8(0x80), code).astype(np.uint8)
+
+
+def quantize_e4m3(x: np.ndarray):
+    """Per-tensor e4m3 quantisation: scale = amax / 448, codes = e4m3(x / scale)."""
+    amax = float(np.max(np.abs(x))) if x.size else 0.0
+    scale = float(np.float32(amax / 448.0)) if amax > 0 else 1.0
+    return e4m3_bits(np.asarray(x, np.float32) / np.float32(scale)), scale
 
 
 def _rms_normalise(x: np.ndarray, eps: float = 1e-6) -> np.ndarray:
