@@ -61,6 +61,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the per-workload timing sweep (eager and CUDA-graph replay)")
+    ap.add_argument("--path", choices=["bf16", "qk8"], default="bf16",
+                    help="bf16: dit.forward; qk8: e4m3 Q/K (RMS-norm + quantising prologue, "
+                         "outside the device-timed region) and dit.forward_qk8")
     return ap.parse_args()
 
 
@@ -488,10 +491,25 @@ def bench_ours(args):
     out = torch.empty_like(q)
     stream = torch.cuda.current_stream(dev)
     flops = w.flops
+    qk8 = args.path == "qk8"
+    if qk8:
+        if not w.rms_norm or w.d != 128:
+            raise SystemExit("--path qk8 needs an RMS-normalised d=128 workload")
+        # |RMS-normalised value| <= sqrt(d): 448/sqrt(d) never saturates e4m3
+        s8 = float(np.float32(math.sqrt(w.d) / 448.0))
+        inv8 = float(np.float32(448.0 / math.sqrt(w.d)))
+        q8 = dit.rmsnorm_e4m3(q, inv8)
+        k8 = dit.rmsnorm_e4m3(k, inv8)
+
+    def fwd():
+        if qk8:
+            dit.forward_qk8(q8, k8, v, s8, s8, w.scale, out=out)
+        else:
+            dit.forward(q, k, v, w.scale, out=out)
 
     # ---- device-resident timing
     for _ in range(max(args.warmup, 3)):
-        dit.forward(q, k, v, w.scale, out=out)
+        fwd()
     torch.cuda.synchronize(dev)
     sampler = ClockSampler(local, pci_bus_id(local))
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
@@ -500,7 +518,7 @@ def bench_ours(args):
     sampler.start()
     ev[0].record(stream)
     for i in range(args.steps):
-        dit.forward(q, k, v, w.scale, out=out)
+        fwd()
         ev[i + 1].record(stream)
     torch.cuda.synchronize(dev)
     sampler.stop()
@@ -520,7 +538,11 @@ def bench_ours(args):
         qd = host[0].to(dev, non_blocking=True)
         kd = host[1].to(dev, non_blocking=True)
         vd = host[2].to(dev, non_blocking=True)
-        o = dit.forward(qd, kd, vd, w.scale)
+        if qk8:
+            o = dit.forward_qk8(dit.rmsnorm_e4m3(qd, inv8), dit.rmsnorm_e4m3(kd, inv8), vd,
+                                s8, s8, w.scale)
+        else:
+            o = dit.forward(qd, kd, vd, w.scale)
         out_host.copy_(o, non_blocking=True)
 
     e2e_step()
@@ -543,29 +565,36 @@ def bench_ours(args):
 
     mean_launch = statistics.mean(per_launch)
     achieved = flops / (mean_launch / 1e3) / 1e12
-    traffic = recorded_traffic(w.name)
+    traffic = recorded_traffic(w.name + ("/qk8" if qk8 else ""))
+    qk_bytes = 1 if qk8 else 2
+    # e4m3 S = Q K^T runs at twice the bf16 rate (nominal ratio), P V at the bf16 rate
+    peak = peaks["bf16"] * (4.0 / 3.0 if qk8 else 1.0)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms / args.steps,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 QK^T, bf16 PV" if qk8 else "bf16",
         "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "Lq": w.Lq, "Lk": w.Lk, "d": w.d,
-                   "segments": dict(w.segments), "parallelism": f"replicas x{world}",
+        "config": {"workload": w.name, "path": args.path, "B": w.B, "H": w.H, "Lq": w.Lq,
+                   "Lk": w.Lk, "d": w.d, "segments": dict(w.segments), "parallelism": f"replicas x{world}",
                    "l2": "inputs 595 MB > 126 MB L2, no flush between steps"
                    if w.name == "2048px_t2i_cfg" else "see workload sizes"},
         "pct_of_peak": 100.0 * value / world / peaks["bf16"],
         "pct_of_sustained_peak": 100.0 * value / world / peaks["bf16_sustained"],
         "ms_per_launch": {"mean": mean_launch, "median": statistics.median(per_launch),
                           "min": min(per_launch)},
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"],
-                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16"], "traffic": traffic,
-                     "peak_source": f"{peaks['source']} dense bf16 burst",
-                     "algorithmic_bytes": 2.0 * (2 * w.B * w.H * w.Lq * w.d
-                                                 + 2 * w.B * w.H * w.Lk * w.d),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peaks['source']} dense bf16 burst"
+                                    + (" x 4/3 (half the flops at the nominal 2x e4m3 rate)"
+                                       if qk8 else ""),
+                     "algorithmic_bytes": float((qk_bytes + 2) * w.B * w.H * w.Lq * w.d
+                                                + (qk_bytes + 2) * w.B * w.H * w.Lk * w.d),
                      "kernel_source": kernel_source_hash()},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
         "gpu_launches": args.steps,
+        "e2e_gpu_launches_per_step": 3 if qk8 else 1,
         "clocks": sampler.summary(),
     }
     if world == 1 and not args.no_sweep:

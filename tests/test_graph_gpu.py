@@ -95,3 +95,38 @@ def test_graph_replay_time_1024px(dit):
     print(f"\n1024px: eager {eager_ms:.4f} ms/call, graph {graph_ms:.4f} ms/call "
           f"({w.flops / graph_ms / 1e9:.0f} TFLOP/s in the graph)")
     assert graph_ms <= eager_ms * 1.05
+
+
+def test_graph_replay_e4m3_pipeline(dit):
+    """The e4m3 path captured as one graph: RMS-norm + e4m3 quantisation of Q
+    and K, then the e4m3-QK forward; replays must equal the eager calls bit
+    for bit."""
+    import torch
+    rng = np.random.default_rng(22)
+    B, H, L, d = 1, 3, 1000, 128
+    q = to_device(W.random_bf16(rng, (B, H, L, d)))
+    k = to_device(W.random_bf16(rng, (B, H, L, d)))
+    v = to_device(W.random_bf16(rng, (B, H, L, d)))
+    s = float(np.float32(math.sqrt(d) / 448))
+    inv = float(np.float32(448 / math.sqrt(d)))
+
+    def pipeline(q8, k8, out):
+        dit.rmsnorm_e4m3(q, inv, out=q8)
+        dit.rmsnorm_e4m3(k, inv, out=k8)
+        dit.forward_qk8(q8, k8, v, s, s, out=out)
+
+    e_q8, e_k8, eager = torch.empty_like(q, dtype=torch.float8_e4m3fn), \
+        torch.empty_like(k, dtype=torch.float8_e4m3fn), torch.empty_like(q)
+    pipeline(e_q8, e_k8, eager)
+    q8, k8, out = torch.empty_like(e_q8), torch.empty_like(e_k8), torch.empty_like(q)
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(st):
+        with torch.cuda.graph(g, stream=st):
+            pipeline(q8, k8, out)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(q8.view(torch.uint8), e_q8.view(torch.uint8))
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
