@@ -44,6 +44,7 @@ FALLBACK_SUSTAINED_TFLOPS = 1400.0
 FALLBACK_HBM_GBS = 6400.0
 KERNEL_SOURCES = ["diffusion_transformer_joint_causal_b300/csrc/dit_attn.cu",
                   "diffusion_transformer_joint_causal_b300/csrc/fmha_pair.cuh",
+                  "diffusion_transformer_joint_causal_b300/csrc/combine.cuh",
                   "diffusion_transformer_joint_causal_b300/csrc/ptx.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fmha_fwd_dram_traffic.txt")
 
@@ -596,6 +597,8 @@ def bench_ours(args):
             tdist.destroy_process_group()
         return 0
 
+    # the attention kernel, plus the merge kernel when the last wave is split
+    launches_per_call = 1 + int(dit.workspace_size(w.B, w.H, w.Lq, w.Lk, w.d, qk8) > 0)
     mean_launch = statistics.mean(per_launch)
     achieved = flops / (mean_launch / 1e3) / 1e12
     traffic = recorded_traffic(w.name + ("/qk8" if qk8 else ""))
@@ -628,8 +631,8 @@ def bench_ours(args):
                 "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                 "overlap": "copies of one step overlap the forward of the previous one "
                            "(two buffer sets, three streams)"},
-        "gpu_launches": args.steps,
-        "e2e_gpu_launches_per_step": 3 if qk8 else 1,
+        "gpu_launches": args.steps * launches_per_call,
+        "e2e_gpu_launches_per_step": launches_per_call + (2 if qk8 else 0),
         "clocks": sampler.summary(),
     }
     if world == 1 and not args.no_sweep:

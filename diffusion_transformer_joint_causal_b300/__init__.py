@@ -25,7 +25,8 @@ import threading
 
 __all__ = ["create", "destroy", "forward", "forward_ptr", "status_string", "get_device_error",
            "check_wait_timeout", "rmsnorm", "rmsnorm_ptr", "forward_qk8", "forward_qk8_ptr",
-           "rmsnorm_e4m3", "rmsnorm_e4m3_ptr",
+           "rmsnorm_e4m3", "rmsnorm_e4m3_ptr", "forward_ws_ptr", "forward_qk8_ws_ptr",
+           "workspace_size",
            "last_cuda_error", "version", "library_path", "DitAttnError", "STATUS",
            "EXPORTED_SYMBOLS"]
 
@@ -40,7 +41,8 @@ STATUS = {
 EXPORTED_SYMBOLS = ("dit_attn_version", "dit_attn_create", "dit_attn_forward",
                     "dit_attn_destroy", "dit_attn_status_string", "dit_attn_get_device_error",
                     "dit_attn_check_wait_timeout", "dit_attn_last_cuda_error", "dit_attn_rmsnorm",
-                    "dit_attn_forward_qk8", "dit_attn_rmsnorm_e4m3")
+                    "dit_attn_forward_qk8", "dit_attn_rmsnorm_e4m3", "dit_attn_forward_ws",
+                    "dit_attn_forward_qk8_ws", "dit_attn_workspace_size")
 
 _lock = threading.Lock()
 _lib = None
@@ -91,6 +93,16 @@ def _load():
             lib.dit_attn_rmsnorm_e4m3.restype = c_int
             lib.dit_attn_rmsnorm_e4m3.argtypes = [vp, vp, vp, ctypes.c_longlong, c_int,
                                                   ctypes.c_float, ctypes.c_float, vp]
+            lib.dit_attn_forward_ws.restype = c_int
+            lib.dit_attn_forward_ws.argtypes = [vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int,
+                                                ctypes.c_float, vp, ctypes.c_longlong, vp]
+            lib.dit_attn_forward_qk8_ws.restype = c_int
+            lib.dit_attn_forward_qk8_ws.argtypes = [vp, vp, vp, vp, c_int, c_int, c_int, c_int,
+                                                    c_int, ctypes.c_float, ctypes.c_float,
+                                                    ctypes.c_float, vp, ctypes.c_longlong, vp]
+            lib.dit_attn_workspace_size.restype = c_int
+            lib.dit_attn_workspace_size.argtypes = [c_int, c_int, c_int, c_int, c_int, c_int,
+                                                    ctypes.POINTER(ctypes.c_longlong)]
             lib.dit_attn_last_cuda_error.restype = c_int
             lib.dit_attn_last_cuda_error.argtypes = []
             _lib = lib
@@ -117,6 +129,7 @@ def create() -> None:
 
 
 def destroy() -> None:
+    _ws_sizes.clear()
     rc = _load().dit_attn_destroy()
     if rc:
         raise DitAttnError(rc, "dit_attn_destroy")
@@ -174,12 +187,64 @@ def _out_like(out, q, shape):
     return out
 
 
-def forward(q, k, v, scale: float | None = None, out=None, stream=None):
+def workspace_size(B: int, H: int, Lq: int, Lk: int, d: int, qk8: bool = False) -> int:
+    """Bytes of split-tail workspace the forward uses for these sizes (0: none)."""
+    nb = ctypes.c_longlong(0)
+    rc = _load().dit_attn_workspace_size(B, H, Lq, Lk, d, int(bool(qk8)), ctypes.byref(nb))
+    if rc:
+        raise DitAttnError(rc, "dit_attn_workspace_size")
+    return nb.value
+
+
+_ws_sizes = {}   # (device index, sizes, qk8) -> workspace bytes; fixed once a device is created
+
+
+def _workspace(workspace, device, B, H, Lq, Lk, d, qk8, stream):
+    """(tensor, pointer, bytes) of the workspace: "auto" allocates what the
+    library asks for through torch's caching allocator, ordered on the stream
+    the call runs on; None runs unsplit; a uint8 CUDA tensor is used as given."""
+    import torch
+    if workspace is None:
+        return None, 0, 0
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError('workspace must be "auto", None or a uint8 CUDA tensor')
+        key = (device.index, B, H, Lq, Lk, d, bool(qk8))
+        nb = _ws_sizes.get(key)
+        if nb is None:   # the caller has made `device` current
+            nb = 0 if d == 64 else workspace_size(B, H, Lq, Lk, d, qk8)
+            _ws_sizes[key] = nb
+        if nb == 0:
+            return None, 0, 0
+        workspace = torch.empty(nb, dtype=torch.uint8, device=device)
+        if stream is not None:
+            # the block returns to the pool only once work on `stream` is done
+            workspace.record_stream(stream if isinstance(stream, torch.cuda.Stream)
+                                    else torch.cuda.ExternalStream(int(stream), device=device))
+    if (not isinstance(workspace, torch.Tensor) or workspace.dtype != torch.uint8
+            or workspace.device != device or not workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous uint8 tensor on the inputs' device")
+    return workspace, workspace.data_ptr(), workspace.numel()
+
+
+def forward_ws_ptr(q: int, k: int, v: int, out: int, B: int, H: int, Lq: int, Lk: int, d: int,
+                   scale: float, workspace: int, workspace_bytes: int, stream=0) -> int:
+    """Raw C-ABI call of dit_attn_forward_ws with integer device pointers; returns the status."""
+    s = stream if isinstance(stream, ctypes.c_void_p) else ctypes.c_void_p(int(stream))
+    return _load().dit_attn_forward_ws(ctypes.c_void_p(q), ctypes.c_void_p(k), ctypes.c_void_p(v),
+                                       ctypes.c_void_p(out), B, H, Lq, Lk, d,
+                                       ctypes.c_float(scale), ctypes.c_void_p(workspace),
+                                       ctypes.c_longlong(workspace_bytes), s)
+
+
+def forward(q, k, v, scale: float | None = None, out=None, stream=None, workspace="auto"):
     """out = softmax(q k^T * scale) v over every (batch, head); bf16 in and out.
 
     q: [B, H, Lq, d], k and v: [B, H, Lk, d], contiguous bf16 CUDA tensors on
     one device; d is 64 or 128; scale defaults to 1/sqrt(d).  Enqueued on
     ``stream`` (default: torch's current stream); returns ``out``.
+    ``workspace``: "auto" (default) gives the split tail the scratch it asks
+    for, None runs without splitting, or pass a uint8 CUDA tensor.
     """
     import torch
     B, H, Lq, Lk, d = _check_qkv(q, k, v, (torch.bfloat16,))
@@ -187,10 +252,12 @@ def forward(q, k, v, scale: float | None = None, out=None, stream=None):
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     with torch.cuda.device(q.device):
-        rc = forward_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                         B, H, Lq, Lk, d, float(scale), _stream_handle(stream))
+        ws, ws_ptr, ws_bytes = _workspace(workspace, q.device, B, H, Lq, Lk, d, False, stream)
+        rc = forward_ws_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                            B, H, Lq, Lk, d, float(scale), ws_ptr, ws_bytes,
+                            _stream_handle(stream))
     if rc:
-        raise DitAttnError(rc, "dit_attn_forward")
+        raise DitAttnError(rc, "dit_attn_forward_ws")
     return out
 
 
@@ -236,13 +303,26 @@ def forward_qk8_ptr(q8: int, k8: int, v: int, out: int, B: int, H: int, Lq: int,
                                         ctypes.c_float(k_scale), s)
 
 
+def forward_qk8_ws_ptr(q8: int, k8: int, v: int, out: int, B: int, H: int, Lq: int, Lk: int,
+                       d: int, scale: float, q_scale: float, k_scale: float, workspace: int,
+                       workspace_bytes: int, stream=0) -> int:
+    """Raw C-ABI call of dit_attn_forward_qk8_ws with integer device pointers."""
+    s = stream if isinstance(stream, ctypes.c_void_p) else ctypes.c_void_p(int(stream))
+    return _load().dit_attn_forward_qk8_ws(ctypes.c_void_p(q8), ctypes.c_void_p(k8),
+                                           ctypes.c_void_p(v), ctypes.c_void_p(out), B, H, Lq,
+                                           Lk, d, ctypes.c_float(scale), ctypes.c_float(q_scale),
+                                           ctypes.c_float(k_scale), ctypes.c_void_p(workspace),
+                                           ctypes.c_longlong(workspace_bytes), s)
+
+
 def forward_qk8(q8, k8, v, q_scale: float, k_scale: float, scale: float | None = None, out=None,
-                stream=None):
+                stream=None, workspace="auto"):
     """out = softmax((q_scale*q8)(k_scale*k8)^T * scale) v with e4m3 q8, k8.
 
     q8: [B, H, Lq, 128], k8: [B, H, Lk, 128], contiguous CUDA tensors of e4m3
     codes (torch.float8_e4m3fn or uint8); v: [B, H, Lk, 128] bf16.  scale
-    defaults to 1/sqrt(d).  Returns the bf16 output ``out``.
+    defaults to 1/sqrt(d); ``workspace`` as for forward.  Returns the bf16
+    output ``out``.
     """
     import torch
     B, H, Lq, Lk, d = _check_qkv(q8, k8, v, (torch.float8_e4m3fn, torch.uint8))
@@ -250,11 +330,12 @@ def forward_qk8(q8, k8, v, q_scale: float, k_scale: float, scale: float | None =
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     with torch.cuda.device(v.device):
-        rc = forward_qk8_ptr(q8.data_ptr(), k8.data_ptr(), v.data_ptr(), out.data_ptr(),
-                             B, H, Lq, Lk, d, float(scale), float(q_scale), float(k_scale),
-                             _stream_handle(stream))
+        ws, ws_ptr, ws_bytes = _workspace(workspace, v.device, B, H, Lq, Lk, d, True, stream)
+        rc = forward_qk8_ws_ptr(q8.data_ptr(), k8.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                B, H, Lq, Lk, d, float(scale), float(q_scale), float(k_scale),
+                                ws_ptr, ws_bytes, _stream_handle(stream))
     if rc:
-        raise DitAttnError(rc, "dit_attn_forward_qk8")
+        raise DitAttnError(rc, "dit_attn_forward_qk8_ws")
     return out
 
 

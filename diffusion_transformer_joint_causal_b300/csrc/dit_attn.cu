@@ -50,10 +50,10 @@ constexpr int kTilesPerUnit = 2;         // query tiles per work unit
 constexpr int kUnitRows = kBM * kTilesPerUnit;
 constexpr int kNumThreads = 384;       // three full warpgroups (setmaxnreg works per warpgroup)
 // Register split: launched at 168 per thread (384 x 168 = 64512); the two
-// softmax warpgroups raise to 224 and the MMA/TMA warpgroup drops to 56:
-// 256 x 224 + 128 x 56 = 64512, exactly the launch's total.
-constexpr int kRegsSoftmax = 224;
-constexpr int kRegsOther = 56;
+// softmax warpgroups raise to 208 and the MMA/TMA warpgroup drops to 88:
+// 256 x 208 + 128 x 88 = 64512, exactly the launch's total.
+constexpr int kRegsSoftmax = 208;
+constexpr int kRegsOther = 88;
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s per wait
@@ -93,10 +93,43 @@ struct Traits {
 struct Params {
   __nv_bfloat16* out;
   int Lq, Lk;
-  int num_qblocks;   // ceil(Lq / 256)
+  int num_qblocks;   // query blocks (work units) per (b,h)
   int num_units;     // B*H*num_qblocks
   float scale_log2;  // scale * log2(e)
+  // Split tail (pair kernel).  Work items [0, split_base) are whole units; each
+  // unit in [split_base, num_units) is cut into `splits` key ranges, items
+  // split_base + c for chunk c < (num_units - split_base) * splits, whose
+  // unnormalised results go to part_o / part_ml for the combine kernel.
+  int split_base;    // num_units when nothing is split
+  int splits;        // 1 when nothing is split
+  int num_items;     // split_base + (num_units - split_base) * splits
+  float* part_o;     // [chunk][512 rows][D] fp32: sum_j p_j v_j against the chunk's max
+  float* part_ml;    // [chunk][512 rows][2] fp32: running max (log2 units), row sum
 };
+
+// One work item: query block `qblock` of head `bh` against key tiles
+// [j0, j1); chunk >= 0 marks a key range of a split unit.
+struct WorkItem {
+  int bh, qblock, j0, j1, chunk;
+};
+
+__device__ __forceinline__ WorkItem work_item(int i, const Params& p, int n_kv) {
+  WorkItem w;
+  int u = i, s = 0;
+  w.chunk = -1;
+  if (i >= p.split_base) {
+    const int c = i - p.split_base;
+    u = p.split_base + c / p.splits;
+    s = c % p.splits;
+    w.chunk = c;
+  }
+  w.bh = u / p.num_qblocks;
+  w.qblock = u % p.num_qblocks;
+  // s < splits <= 16 and n_kv < 2^24, so the products fit in 32 bits
+  w.j0 = w.chunk < 0 ? 0 : s * n_kv / p.splits;
+  w.j1 = w.chunk < 0 ? n_kv : (s + 1) * n_kv / p.splits;
+  return w;
+}
 
 struct Shared {
   uint32_t base;          // shared-window address of the aligned base
@@ -446,6 +479,25 @@ __device__ __forceinline__ void softmax_tile_half(uint32_t taddr_s, int key0, bo
   l += sum8(acc);
 }
 
+// A chunk of a split unit: this thread's D/2 unnormalised output columns of
+// partial row prow, and (from the first half) the row's running max and sum.
+template <int D>
+__device__ __forceinline__ void store_partial(const Params& p, int64_t prow, int half,
+                                           uint32_t taddr_o, float m_used, float l_row) {
+  float4* po = reinterpret_cast<float4*>(p.part_o + prow * D + half * (D / 2));
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) {
+    uint32_t o[32];
+    tmem_ld16x2_32<D / 2>(taddr_o + c * 32, o);
+    tmem_wait_ld();
+#pragma unroll
+    for (int v = 0; v < 8; ++v)
+      po[c * 8 + v] = make_float4(__uint_as_float(o[4 * v]), __uint_as_float(o[4 * v + 1]),
+                                  __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3]));
+  }
+  if (half == 0) reinterpret_cast<float2*>(p.part_ml)[prow] = make_float2(m_used, l_row);
+}
+
 // kPair: the CTA is one half of a pair; a work unit then spans 512 query rows
 // (this CTA's 256 start at rank*256) and P-ready is reported on the barrier of
 // the pair's leader CTA, whose warp issues the MMAs.  Each warp arrives once
@@ -470,12 +522,13 @@ __device__ void softmax_role(const Params& p, const Shared& sh, uint32_t tmem) {
   const int unit_rows = kPair ? 2 * kUnitRows : kUnitRows;
   const uint32_t p_full_leader0 = kPair ? mapa_shared(sh.bar(T::kBarPFull), 0) : 0u;
 
-  for (int u = u0; u < p.num_units && ok; u += u_stride, ++it) {
-    const int bh = u / p.num_qblocks;
-    const int row_base = (u % p.num_qblocks) * unit_rows + rank * kUnitRows + r;
+  for (int i = u0; i < p.num_items && ok; i += u_stride, ++it) {
+    const WorkItem w = work_item(i, p, n_kv);
+    const int bh = w.bh;
+    const int row_base = w.qblock * unit_rows + rank * kUnitRows + r;
     float m_used[2] = {-INFINITY, -INFINITY};   // running max, in units of s*scale*log2(e)
     float l[2] = {0.f, 0.f};                     // this half-row's share of the row sum
-    for (int j = 0; j < n_kv && ok; ++j, ++g) {
+    for (int j = w.j0; j < w.j1 && ok; ++j, ++g) {
       const bool masked = (j == n_kv - 1) && (tail < kBN);
       const int valid = masked ? tail : kBN;
 #pragma unroll
@@ -486,7 +539,7 @@ __device__ void softmax_role(const Params& p, const Shared& sh, uint32_t tmem) {
         // O_t is quiescent here: S_t's completion implies the previous P.V
         // product into O_t finished.
         const uint32_t taddr_o = lane_addr + T::col_o(t);
-        softmax_tile_half<D>(lane_addr + T::col_s(t), key0, j == 0, masked, valid, scale_log2,
+        softmax_tile_half<D>(lane_addr + T::col_s(t), key0, j == w.j0, masked, valid, scale_log2,
                              m_used[t], l[t], [&](float f) { rescale_o_half<D>(taddr_o, f); });
         tmem_wait_st();
         tc_fence_before();
@@ -499,12 +552,19 @@ __device__ void softmax_role(const Params& p, const Shared& sh, uint32_t tmem) {
     }
     if (!ok) break;
     // Epilogue: O_t / l -> bf16 -> global; each thread writes its D/2 columns.
+    // A chunk of a split unit stores O_t, its max and row sum unnormalised.
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       const bool got = mbar_wait(sh.bar(T::kBarOFull + t), it & 1u, kWaitLimitNs, sh.abort);
       if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
       tc_fence_after();
       const float l_row = l[t] + __shfl_xor_sync(0xffffffffu, l[t], 16);
+      if (kPair && w.chunk >= 0) {
+        const int64_t prow = static_cast<int64_t>(w.chunk) * (2 * kUnitRows) + rank * kUnitRows +
+                             t * kBM + r;
+        store_partial<D>(p, prow, half, lane_addr + T::col_o(t), m_used[t], l_row);
+        continue;
+      }
       const float inv_l = 1.f / l_row;
       const int row = row_base + t * kBM;
       const bool row_ok = row < p.Lq;
@@ -620,6 +680,7 @@ __global__ void wait_timeout_kernel(uint64_t limit_ns) {
 }  // namespace dit
 
 #include "fmha_pair.cuh"
+#include "combine.cuh"
 #include "rmsnorm.cuh"
 
 // =================================================================== host side
@@ -699,6 +760,11 @@ int launch(const void* q, const void* k, const void* v, void* out, int64_t BH, i
   p.num_qblocks = (Lq + dit::kUnitRows - 1) / dit::kUnitRows;
   p.num_units = static_cast<int>(BH * p.num_qblocks);
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.split_base = p.num_units;
+  p.splits = 1;
+  p.num_items = p.num_units;
+  p.part_o = nullptr;
+  p.part_ml = nullptr;
   const int grid = p.num_units < num_sms ? p.num_units : num_sms;
   dit::fmha_fwd_kernel<D><<<grid, dit::kNumThreads, Traits<D>::kSmemBytes, stream>>>(tq, tk, tv, p);
   const cudaError_t e = cudaGetLastError();
@@ -722,12 +788,44 @@ cudaLaunchConfig_t pair_launch_config(int grid, cudaStream_t stream, cudaLaunchA
   return cfg;
 }
 
+// Split tail of the pair kernel.  A persistent launch of P clusters runs the
+// units in waves of P; when the last wave is partial (rem = units mod P > 0),
+// its units are cut into `splits` key ranges so that the wave fills the GPU,
+// each range at least kMinTilesPerChunk key tiles long (a chunk writes 260 KB
+// of partial results, about one key tile's worth of time).
+constexpr int kMinTilesPerChunk = 8;
+constexpr int kMaxSplits = 16;
+constexpr int kPairUnitRows = 2 * dit::kUnitRows;
+
+struct SplitPlan {
+  int split_base, splits, num_items;
+  int64_t chunks;     // (num_units - split_base) * splits
+  int64_t ws_bytes;   // partial O and (max, sum) of every chunk
+};
+
+SplitPlan plan_split(int64_t num_units, int n_kv, int max_pairs) {
+  SplitPlan s = {static_cast<int>(num_units), 1, static_cast<int>(num_units), 0, 0};
+  const int64_t rem = num_units % max_pairs;
+  if (rem == 0) return s;
+  int64_t splits = max_pairs / rem;
+  if (splits > n_kv / kMinTilesPerChunk) splits = n_kv / kMinTilesPerChunk;
+  if (splits > kMaxSplits) splits = kMaxSplits;
+  if (splits < 2) return s;
+  s.split_base = static_cast<int>(num_units - rem);
+  s.splits = static_cast<int>(splits);
+  s.chunks = rem * splits;
+  s.num_items = static_cast<int>(s.split_base + s.chunks);
+  s.ws_bytes = s.chunks * kPairUnitRows * (128 + 2) * static_cast<int64_t>(sizeof(float));
+  return s;
+}
+
 // d = 128: clusters of two CTAs, one work unit = 512 query rows.  With kQK8,
 // q and k hold e4m3 bytes and `scale` already includes their dequantisation
-// scales.
+// scales.  With a workspace of at least the plan's size the last, partial wave
+// runs split, followed by the combine kernel on the same stream.
 template <bool kQK8>
 int launch_pair(const void* q, const void* k, const void* v, void* out, int64_t BH, int Lq, int Lk,
-                double scale, cudaStream_t stream, int max_pairs) {
+                double scale, cudaStream_t stream, int max_pairs, void* ws, int64_t ws_bytes) {
   CUtensorMap tq, tk, tv;
   int rc;
   const int qk_bytes = kQK8 ? 1 : 2;
@@ -738,15 +836,31 @@ int launch_pair(const void* q, const void* k, const void* v, void* out, int64_t 
   p.out = static_cast<__nv_bfloat16*>(out);
   p.Lq = Lq;
   p.Lk = Lk;
-  p.num_qblocks = (Lq + 2 * dit::kUnitRows - 1) / (2 * dit::kUnitRows);
+  p.num_qblocks = (Lq + kPairUnitRows - 1) / kPairUnitRows;
   p.num_units = static_cast<int>(BH * p.num_qblocks);
   p.scale_log2 = static_cast<float>(scale * 1.4426950408889634);
-  const int pairs = p.num_units < max_pairs ? p.num_units : max_pairs;
+  SplitPlan plan = plan_split(p.num_units, (Lk + dit::kBN - 1) / dit::kBN, max_pairs);
+  if (plan.splits > 1 && (!ws || ws_bytes < plan.ws_bytes))
+    plan = SplitPlan{p.num_units, 1, p.num_units, 0, 0};
+  p.split_base = plan.split_base;
+  p.splits = plan.splits;
+  p.num_items = plan.num_items;
+  p.part_o = plan.splits > 1 ? static_cast<float*>(ws) : nullptr;
+  p.part_ml = plan.splits > 1 ? p.part_o + plan.chunks * kPairUnitRows * 128 : nullptr;
+  const int pairs = p.num_items < max_pairs ? p.num_items : max_pairs;
   cudaLaunchAttribute attr;
   cudaLaunchConfig_t cfg =
       pair_launch_config(2 * pairs, stream, &attr, dit::PairTraitsT<kQK8>::kSmemBytes);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, dit::fmha_fwd_pair_kernel<kQK8>, tq, tk, tv, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, dit::fmha_fwd_pair_kernel<kQK8>, tq, tk, tv, p);
   if (e != cudaSuccess) return cuda_fail(e);
+  if (plan.splits > 1) {
+    const int64_t rows = (plan.num_items - plan.split_base) / plan.splits * int64_t{kPairUnitRows};
+    const int64_t blocks = (rows * 32 + 255) / 256;
+    dit::combine_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        p.part_o, p.part_ml, p.out, p.split_base, p.splits, p.num_qblocks, p.Lq, rows);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
   return DIT_ATTN_OK;
 }
 
@@ -791,6 +905,23 @@ int check_forward_args(const void* q, const void* k, const void* v, const void* 
   const int64_t q_bytes = BH * Lq * d * qk_bytes, k_bytes = BH * Lk * d * qk_bytes;
   if (overlaps(out, o_bytes, q, q_bytes) || overlaps(out, o_bytes, k, k_bytes) ||
       overlaps(out, o_bytes, v, v_bytes))
+    return DIT_ATTN_ERR_INVALID_ARG;
+  return DIT_ATTN_OK;
+}
+
+// The optional workspace of the split tail: 16-byte aligned, non-negative size,
+// no overlap with the tensors (NULL with size 0 runs unsplit).
+int check_workspace(const void* ws, long long ws_bytes, const void* q, const void* k,
+                    const void* v, const void* out, int B, int H, int Lq, int Lk, int d,
+                    int qk_bytes) {
+  if (ws_bytes < 0 || (ws_bytes > 0 && !ws)) return DIT_ATTN_ERR_INVALID_ARG;
+  if (!ws || ws_bytes == 0) return DIT_ATTN_OK;
+  if (reinterpret_cast<uintptr_t>(ws) & 15u) return DIT_ATTN_ERR_INVALID_ARG;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  const int64_t o_bytes = BH * Lq * d * 2, v_bytes = BH * Lk * d * 2;
+  const int64_t q_bytes = BH * Lq * d * qk_bytes, k_bytes = BH * Lk * d * qk_bytes;
+  if (overlaps(ws, ws_bytes, q, q_bytes) || overlaps(ws, ws_bytes, k, k_bytes) ||
+      overlaps(ws, ws_bytes, v, v_bytes) || overlaps(ws, ws_bytes, out, o_bytes))
     return DIT_ATTN_ERR_INVALID_ARG;
   return DIT_ATTN_OK;
 }
@@ -861,9 +992,12 @@ int dit_attn_destroy(void) {
   return DIT_ATTN_OK;
 }
 
-int dit_attn_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int Lq,
-                     int Lk, int d, float scale, void* stream) {
-  const int rc = check_forward_args(q, k, v, out, B, H, Lq, Lk, d, scale, 2);
+int dit_attn_forward_ws(const void* q, const void* k, const void* v, void* out, int B, int H,
+                        int Lq, int Lk, int d, float scale, void* workspace,
+                        long long workspace_bytes, void* stream) {
+  int rc = check_forward_args(q, k, v, out, B, H, Lq, Lk, d, scale, 2);
+  if (rc != DIT_ATTN_OK) return rc;
+  rc = check_workspace(workspace, workspace_bytes, q, k, v, out, B, H, Lq, Lk, d, 2);
   if (rc != DIT_ATTN_OK) return rc;
   const int64_t BH = static_cast<int64_t>(B) * H;
   int dev = -1;
@@ -877,12 +1011,19 @@ int dit_attn_forward(const void* q, const void* k, const void* v, void* out, int
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return d == 64 ? launch<64>(q, k, v, out, BH, Lq, Lk, scale, s, num_sms)
-                 : launch_pair<false>(q, k, v, out, BH, Lq, Lk, scale, s, max_pairs);
+                 : launch_pair<false>(q, k, v, out, BH, Lq, Lk, scale, s, max_pairs, workspace,
+                                      workspace_bytes);
 }
 
-int dit_attn_forward_qk8(const void* q8, const void* k8, const void* v, void* out, int B, int H,
-                         int Lq, int Lk, int d, float scale, float q_scale, float k_scale,
-                         void* stream) {
+int dit_attn_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int Lq,
+                     int Lk, int d, float scale, void* stream) {
+  return dit_attn_forward_ws(q, k, v, out, B, H, Lq, Lk, d, scale, nullptr, 0, stream);
+}
+
+int dit_attn_forward_qk8_ws(const void* q8, const void* k8, const void* v, void* out, int B,
+                            int H, int Lq, int Lk, int d, float scale, float q_scale,
+                            float k_scale, void* workspace, long long workspace_bytes,
+                            void* stream) {
   int rc = check_forward_args(q8, k8, v, out, B, H, Lq, Lk, d, scale, 1);
   if (rc != DIT_ATTN_OK) return rc;
   if (!std::isfinite(q_scale) || !std::isfinite(k_scale) || q_scale < 0.f || k_scale < 0.f)
@@ -890,6 +1031,8 @@ int dit_attn_forward_qk8(const void* q8, const void* k8, const void* v, void* ou
   const double logit_scale = static_cast<double>(scale) * q_scale * k_scale;
   if (!(logit_scale <= 3.0e38)) return DIT_ATTN_ERR_INVALID_ARG;
   if (d != 128) return DIT_ATTN_ERR_UNSUPPORTED;
+  rc = check_workspace(workspace, workspace_bytes, q8, k8, v, out, B, H, Lq, Lk, d, 1);
+  if (rc != DIT_ATTN_OK) return rc;
   const int64_t BH = static_cast<int64_t>(B) * H;
   int dev = -1;
   if (!current_device(&dev)) return DIT_ATTN_ERR_NO_DEVICE;
@@ -900,7 +1043,40 @@ int dit_attn_forward_qk8(const void* q8, const void* k8, const void* v, void* ou
     max_pairs = g_state[dev].max_pairs_qk8;
   }
   return launch_pair<true>(q8, k8, v, out, BH, Lq, Lk, logit_scale,
-                           static_cast<cudaStream_t>(stream), max_pairs);
+                           static_cast<cudaStream_t>(stream), max_pairs, workspace,
+                           workspace_bytes);
+}
+
+int dit_attn_forward_qk8(const void* q8, const void* k8, const void* v, void* out, int B, int H,
+                         int Lq, int Lk, int d, float scale, float q_scale, float k_scale,
+                         void* stream) {
+  return dit_attn_forward_qk8_ws(q8, k8, v, out, B, H, Lq, Lk, d, scale, q_scale, k_scale,
+                                 nullptr, 0, stream);
+}
+
+int dit_attn_workspace_size(int B, int H, int Lq, int Lk, int d, int qk8, long long* bytes) {
+  if (!bytes) return DIT_ATTN_ERR_INVALID_ARG;
+  *bytes = 0;
+  if (B < 1 || H < 1 || Lq < 1 || Lk < 1) return DIT_ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return DIT_ATTN_ERR_UNSUPPORTED;
+  if (qk8 && d != 128) return DIT_ATTN_ERR_UNSUPPORTED;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  const int64_t qblocks = (static_cast<int64_t>(Lq) + dit::kUnitRows - 1) / dit::kUnitRows;
+  if (BH > INT_MAX || Lq > INT_MAX - 2 * dit::kUnitRows || Lk > INT_MAX - 2 * dit::kUnitRows ||
+      BH * qblocks > INT_MAX)
+    return DIT_ATTN_ERR_UNSUPPORTED;
+  int dev = -1;
+  if (!current_device(&dev)) return DIT_ATTN_ERR_NO_DEVICE;
+  int max_pairs;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_state[dev].ready) return DIT_ATTN_ERR_NOT_INITIALIZED;
+    max_pairs = qk8 ? g_state[dev].max_pairs_qk8 : g_state[dev].max_pairs;
+  }
+  if (d == 64) return DIT_ATTN_OK;   // the d = 64 kernel never splits
+  const int64_t units = BH * ((static_cast<int64_t>(Lq) + kPairUnitRows - 1) / kPairUnitRows);
+  *bytes = plan_split(units, (Lk + dit::kBN - 1) / dit::kBN, max_pairs).ws_bytes;
+  return DIT_ATTN_OK;
 }
 
 int dit_attn_check_wait_timeout(int limit_us, void* stream) {

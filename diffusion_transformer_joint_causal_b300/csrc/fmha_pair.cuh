@@ -95,12 +95,13 @@ __device__ void pair_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
     if (++stage == T::kStages) { stage = 0; phase ^= 1u; }
   };
 
-  for (int u = static_cast<int>(cluster_id_x()); u < p.num_units && ok;
-       u += static_cast<int>(num_clusters_x()), ++it) {
-    const int bh = u / p.num_qblocks;
-    const int row0 = (u % p.num_qblocks) * (2 * kUnitRows) + static_cast<int>(rank) * kUnitRows;
+  for (int i = static_cast<int>(cluster_id_x()); i < p.num_items && ok;
+       i += static_cast<int>(num_clusters_x()), ++it) {
+    const WorkItem w = work_item(i, p, n_kv);
+    const int bh = w.bh;
+    const int row0 = w.qblock * (2 * kUnitRows) + static_cast<int>(rank) * kUnitRows;
     ok = load_q(0, bh, row0);
-    for (int j = 0; j < n_kv && ok; ++j) {
+    for (int j = w.j0; j < w.j1 && ok; ++j) {
       // K half: keys j*128 + 64*rank .. +63, all d columns (128-byte boxes)
       ok = take_empty(T::kKHalfBytes);
       if (!ok) break;
@@ -111,7 +112,7 @@ __device__ void pair_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                            j * kBN + static_cast<int>(rank) * 64, bh, pol_kv);
       }
       advance();
-      if (j == 0) {
+      if (j == w.j0) {
         ok = load_q(1, bh, row0);
         if (!ok) break;
       }
@@ -207,8 +208,13 @@ __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) 
   // the warp waits for P_1 anyway, off the path from P-ready to the next MMA.
   // Commits follow the MMA block they track (a commit between MMAs stalls
   // the issuing thread).
-  for (int u = static_cast<int>(cluster_id_x()); u < p.num_units && ok;
-       u += static_cast<int>(num_clusters_x()), ++it) {
+  for (int i = static_cast<int>(cluster_id_x()); i < p.num_items && ok;
+       i += static_cast<int>(num_clusters_x()), ++it) {
+    int n = n_kv;                // key tiles of this item
+    if (i >= p.split_base) {
+      const int s = (i - p.split_base) % p.splits;
+      n = (s + 1) * n_kv / p.splits - s * n_kv / p.splits;
+    }
     uint32_t sK = 0, sV = 0, sK_next = 0, sV_next = 0;
     ok = wait(T::kBarQFull + 0, it & 1u) && take_stage(sK);
     if (!ok) break;
@@ -216,23 +222,23 @@ __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) 
     if (issuer) {
       pair_issue_qk<kQK8>(tmem + T::col_s(0), q_lo0, kv_lo(sK));
       mma_commit_pair(sh.bar(T::kBarSFull + 0), kBoth);
-      if (n_kv == 1) mma_commit_pair(sh.bar(T::kBarQEmpty + 0), kBoth);
+      if (n == 1) mma_commit_pair(sh.bar(T::kBarQEmpty + 0), kBoth);
     }
     __syncwarp();
-    ok = wait(T::kBarQFull + 1, it & 1u) && take_stage(sV) && (n_kv == 1 || take_stage(sK_next));
+    ok = wait(T::kBarQFull + 1, it & 1u) && take_stage(sV) && (n == 1 || take_stage(sK_next));
     if (!ok) break;
     tc_fence_after();
     if (issuer) {
       pair_issue_qk<kQK8>(tmem + T::col_s(1), q_lo1, kv_lo(sK));
       mma_commit_pair(sh.bar(T::kBarSFull + 1), kBoth);
-      if (n_kv == 1) mma_commit_pair(sh.bar(T::kBarQEmpty + 1), kBoth);
+      if (n == 1) mma_commit_pair(sh.bar(T::kBarQEmpty + 1), kBoth);
       mma_commit_pair(sh.bar(T::kBarEmpty + sK), kBoth);
     }
     __syncwarp();
 
-    for (int j = 0; j < n_kv && ok; ++j, ++g) {
-      // held: sV = V(j); sK_next = K(j+1) when j+1 < n_kv
-      const bool more = j + 1 < n_kv;
+    for (int j = 0; j < n && ok; ++j, ++g) {   // j: tile index within the item
+      // held: sV = V(j); sK_next = K(j+1) when j+1 < n
+      const bool more = j + 1 < n;
       ok = wait(T::kBarPFull + 0, g & 1u);
       if (!ok) break;
       tc_fence_after();
@@ -241,13 +247,13 @@ __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) 
         if (more) {
           pair_issue_qk<kQK8>(tmem + T::col_s(0), q_lo0, kv_lo(sK_next));
           mma_commit_pair(sh.bar(T::kBarSFull + 0), kBoth);
-          if (j + 2 == n_kv) mma_commit_pair(sh.bar(T::kBarQEmpty + 0), kBoth);
+          if (j + 2 == n) mma_commit_pair(sh.bar(T::kBarQEmpty + 0), kBoth);
         } else {
           mma_commit_pair(sh.bar(T::kBarOFull + 0), kBoth);
         }
       }
       __syncwarp();
-      if (more) ok = take_stage(sV_next) && (j + 2 >= n_kv || take_stage(sK));
+      if (more) ok = take_stage(sV_next) && (j + 2 >= n || take_stage(sK));
       ok = ok && wait(T::kBarPFull + 1, g & 1u);
       if (!ok) break;
       tc_fence_after();
@@ -257,7 +263,7 @@ __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) 
           pair_issue_qk<kQK8>(tmem + T::col_s(1), q_lo1, kv_lo(sK_next));
           mma_commit_pair(sh.bar(T::kBarEmpty + sV), kBoth);
           mma_commit_pair(sh.bar(T::kBarSFull + 1), kBoth);
-          if (j + 2 == n_kv) mma_commit_pair(sh.bar(T::kBarQEmpty + 1), kBoth);
+          if (j + 2 == n) mma_commit_pair(sh.bar(T::kBarQEmpty + 1), kBoth);
           mma_commit_pair(sh.bar(T::kBarEmpty + sK_next), kBoth);
         } else {
           mma_commit_pair(sh.bar(T::kBarEmpty + sV), kBoth);

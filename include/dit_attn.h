@@ -16,7 +16,7 @@
  * The text, image and reference-image tokens of a DiT block form one
  * sequence; every query sees every key.
  *
- * Tensors (all owned by the caller; the library never allocates per call):
+ * Tensors (all owned by the caller; the library never allocates):
  *   q   : device pointer, bf16, contiguous [B, H, Lq, d]
  *   k, v: device pointers, bf16, contiguous [B, H, Lk, d]
  *   out : device pointer, bf16, contiguous [B, H, Lq, d]; written, never read
@@ -76,6 +76,33 @@ int dit_attn_forward(const void* q, const void* k, const void* v, void* out, int
                      int Lk, int d, float scale, void* stream);
 
 /*
+ * dit_attn_forward with a caller-owned workspace for the split tail.  A
+ * persistent launch runs the 512-row work units in waves of one unit per CTA
+ * pair; when the last wave is partial, its units are cut into key ranges
+ * whose unnormalised partial results (output, running max, row sum) go to the
+ * workspace and are merged by a second kernel on the same stream, so the last
+ * wave fills the GPU.  The result equals dit_attn_forward's within rounding
+ * (not bit for bit: the partial sums are added in another order).
+ *   workspace: device pointer, 16-byte aligned, must not overlap q, k, v or
+ *              out; NULL with workspace_bytes 0 runs without splitting.
+ *   workspace_bytes: its size; when smaller than dit_attn_workspace_size
+ *              reports, the call runs without splitting.
+ * The workspace is scratch for this call only: calls that may overlap (other
+ * streams) need separate workspaces.  Otherwise as dit_attn_forward.
+ */
+int dit_attn_forward_ws(const void* q, const void* k, const void* v, void* out, int B, int H,
+                        int Lq, int Lk, int d, float scale, void* workspace,
+                        long long workspace_bytes, void* stream);
+
+/*
+ * Workspace bytes that dit_attn_forward_ws (qk8 = 0) or dit_attn_forward_qk8_ws
+ * (qk8 = 1) uses for these sizes on the current device; 0 when no split
+ * applies (d = 64, or the last wave is full or its units too short).  Size
+ * arguments as for the forward calls; requires dit_attn_create().
+ */
+int dit_attn_workspace_size(int B, int H, int Lq, int Lk, int d, int qk8, long long* bytes);
+
+/*
  * The same attention with e4m3 queries and keys ("cuDNN FP8 attention" is the
  * FP8 attention that "Speed Up Image Generation with FLUX 3 Image Klein on
  * NVIDIA Blackwell GPUs" (Key takeaways, fourth item) and the sns.style
@@ -102,6 +129,12 @@ int dit_attn_forward(const void* q, const void* k, const void* v, void* out, int
 int dit_attn_forward_qk8(const void* q8, const void* k8, const void* v, void* out, int B, int H,
                          int Lq, int Lk, int d, float scale, float q_scale, float k_scale,
                          void* stream);
+
+/* dit_attn_forward_qk8 with a workspace, as dit_attn_forward_ws. */
+int dit_attn_forward_qk8_ws(const void* q8, const void* k8, const void* v, void* out, int B,
+                            int H, int Lq, int Lk, int d, float scale, float q_scale,
+                            float k_scale, void* workspace, long long workspace_bytes,
+                            void* stream);
 
 /*
  * RMS normalisation of queries or keys over the head dimension, per token and

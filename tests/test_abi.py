@@ -188,3 +188,43 @@ def test_python_e4m3_wrappers_check_tensors():
         dit.forward_qk8(x, x, x, 1.0, 1.0)                # bf16 q8 / CPU tensors
     with pytest.raises(TypeError):
         dit.rmsnorm_e4m3(x, 1.0)                          # CPU tensor
+
+
+WS = A + 8 * MB   # a fake, aligned workspace address clear of the fake tensors
+
+
+@pytest.mark.parametrize("ws,nbytes,expect", [
+    (WS, -1, 1),                 # negative size
+    (0, 4096, 1),                # size without a pointer
+    (WS + 8, 4096, 1),           # misaligned
+    (A + 2 * MB, 4096, 1),       # overlaps v
+    (A + 3 * MB + 512, 64, 1),   # overlaps out (8*64*2 bytes from A + 3 MB)
+])
+def test_forward_ws_rejects_bad_workspace(ws, nbytes, expect):
+    args = (A, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 8, 8, 64, 0.125)
+    assert dit.forward_ws_ptr(*args, ws, nbytes) == expect
+    qk8 = (A, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 8, 8, 128, 0.125, 0.02, 0.03)
+    assert dit.forward_qk8_ws_ptr(*qk8, ws, nbytes) == expect
+
+
+def test_forward_ws_still_checks_tensors():
+    assert dit.forward_ws_ptr(0, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 8, 8, 64, 0.125, WS, 4096) == 1
+    assert dit.forward_ws_ptr(A, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 8, 8, 96, 0.125, WS, 4096) == 2
+
+
+def test_workspace_size_validates_before_cuda():
+    lib = ctypes.CDLL(dit.library_path())
+    lib.dit_attn_workspace_size.argtypes = [ctypes.c_int] * 6 + [ctypes.c_void_p]
+    nb = ctypes.c_longlong(7)
+    assert lib.dit_attn_workspace_size(1, 1, 8, 8, 128, 0, None) == 1            # no output pointer
+    assert lib.dit_attn_workspace_size(0, 1, 8, 8, 128, 0, ctypes.byref(nb)) == 1 and nb.value == 0
+    assert lib.dit_attn_workspace_size(1, 1, 8, 8, 96, 0, ctypes.byref(nb)) == 2
+    assert lib.dit_attn_workspace_size(1, 1, 8, 8, 64, 1, ctypes.byref(nb)) == 2  # e4m3 is d=128 only
+
+
+@pytest.mark.skipif(_has_gpu(), reason="checks the no-device path")
+def test_workspace_entry_points_no_device():
+    assert dit.forward_ws_ptr(A, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 8, 8, 64, 0.125, WS, 4096) == 4
+    assert dit.forward_ws_ptr(A, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 8, 8, 64, 0.125, 0, 0) == 4
+    with pytest.raises(dit.DitAttnError):
+        dit.workspace_size(1, 24, 16896, 16896, 128)

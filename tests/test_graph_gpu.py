@@ -130,3 +130,27 @@ def test_graph_replay_e4m3_pipeline(dit):
     torch.cuda.synchronize()
     assert torch.equal(q8.view(torch.uint8), e_q8.view(torch.uint8))
     assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+
+
+def test_graph_replay_split_tail(dit):
+    """A call whose work units are split over key ranges (attention kernel,
+    then the merge kernel, workspace from the capture's memory pool) replays
+    bit for bit."""
+    import torch
+    B, H, Lq, Lk, d = 1, 2, 900, 6000, 128
+    assert dit.workspace_size(B, H, Lq, Lk, d) > 0
+    rng = np.random.default_rng(23)
+    q, k, v = (to_device(W.random_bf16(rng, (B, H, L, d))) for L in (Lq, Lk, Lk))
+    eager = dit.forward(q, k, v, 0.088)
+    out = torch.empty_like(q)
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(st):
+        with torch.cuda.graph(g, stream=st):
+            dit.forward(q, k, v, 0.088, out=out)
+    torch.cuda.synchronize()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))

@@ -186,3 +186,67 @@ def test_output_rows_past_lq_untouched(dit):
     dit.forward(q, k, v, 0.125, out=out)
     torch.cuda.synchronize()
     assert torch.all(buf[77 * 64:] == 7.0)
+
+
+# Split tail: the last, partial wave of work units is cut into key ranges whose
+# partial results a second kernel merges.  Shapes with fewer units than CTA
+# pairs split every unit (2 to 8 ranges); each must match the oracle element by
+# element and the unsplit call within the same tolerance.
+SPLIT_SHAPES = [
+    # (B, H, Lq, Lk, d)
+    (1, 1, 700, 4000, 128),
+    (1, 3, 1100, 2500, 128),
+    (2, 2, 513, 8192, 128),
+    (1, 1, 1, 3000, 128),
+]
+
+
+@pytest.mark.parametrize("shape", SPLIT_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_split_tail_every_element(dit, shape):
+    import torch
+    B, H, Lq, Lk, d = shape
+    assert dit.workspace_size(B, H, Lq, Lk, d) > 0        # the split path is taken
+    rng = np.random.default_rng(2000 + Lq + Lk)
+    q = W.random_bf16(rng, (B, H, Lq, d))
+    k = W.random_bf16(rng, (B, H, Lk, d))
+    v = W.random_bf16(rng, (B, H, Lk, d))
+    scale = float(np.float32(1 / math.sqrt(d)))
+    qd, kd, vd = to_device(q), to_device(k), to_device(v)
+    split = dit.forward(qd, kd, vd, scale)                  # workspace="auto"
+    whole = dit.forward(qd, kd, vd, scale, workspace=None)
+    torch.cuda.synchronize()
+    got = to_host_f64(split)
+    assert_close(got, oracle_full(q, k, v, scale), f"split {shape}")
+    assert_close(got, to_host_f64(whole), f"split vs unsplit {shape}")
+
+
+def test_split_tail_explicit_workspace_and_rows_past_lq(dit):
+    # A caller-owned workspace inside a larger buffer; rows past Lq untouched.
+    import torch
+    B, H, Lq, Lk, d = 1, 2, 300, 5000, 128
+    nb = dit.workspace_size(B, H, Lq, Lk, d)
+    assert nb > 0
+    rng = np.random.default_rng(2100)
+    q = W.random_bf16(rng, (B, H, Lq, d))
+    k = W.random_bf16(rng, (B, H, Lk, d))
+    v = W.random_bf16(rng, (B, H, Lk, d))
+    ws = torch.empty(nb + 4096, dtype=torch.uint8, device="cuda")
+    buf = torch.full((B * H * Lq * d + 4096,), 7.0, dtype=torch.bfloat16, device="cuda")
+    out = buf[: B * H * Lq * d].view(B, H, Lq, d)
+    scale = float(np.float32(1 / math.sqrt(d)))
+    dit.forward(to_device(q), to_device(k), to_device(v), scale, out=out, workspace=ws[16:16 + nb])
+    torch.cuda.synchronize()
+    assert torch.all(buf[B * H * Lq * d:] == 7.0)
+    assert_close(to_host_f64(out), oracle_full(q, k, v, scale), "explicit workspace")
+
+
+def test_split_tail_short_workspace_runs_unsplit(dit):
+    import torch
+    B, H, Lq, Lk, d = 1, 1, 700, 4000, 128
+    rng = np.random.default_rng(2200)
+    q, k, v = (to_device(W.random_bf16(rng, (B, H, L, d))) for L in (Lq, Lk, Lk))
+    small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    a = dit.forward(q, k, v, 0.088, workspace=small)
+    b = dit.forward(q, k, v, 0.088, workspace=None)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))

@@ -248,3 +248,16 @@ def test_rmsnorm_e4m3_then_forward_qk8(dit):
     want = oracle.attention(qd.astype(np.float64) * s, kd.astype(np.float64) * s,
                             W.bf16_to_f32(v).astype(np.float64), w.scale)
     assert_close(got, want, "rmsnorm_e4m3 + forward_qk8")
+
+
+def test_split_tail_e4m3(dit):
+    # fewer work units than CTA pairs: every unit is split over key ranges
+    B, H, Lq, Lk = 1, 2, 900, 6000
+    assert dit.workspace_size(B, H, Lq, Lk, 128, qk8=True) > 0
+    rng = np.random.default_rng(35)
+    q8, qs, qd = quantise(W.random_bf16(rng, (B, H, Lq, 128)))
+    k8, ks, kd = quantise(W.random_bf16(rng, (B, H, Lk, 128)))
+    v = W.random_bf16(rng, (B, H, Lk, 128))
+    got = to_host_f64(run_qk8(dit, q8, k8, v, qs, ks, 0.088))
+    want = oracle.attention(qd, kd, W.bf16_to_f32(v).astype(np.float64), 0.088)
+    assert_close(got, want, "e4m3 split tail")
