@@ -26,7 +26,7 @@ import threading
 __all__ = ["create", "destroy", "forward", "forward_ptr", "status_string", "get_device_error",
            "check_wait_timeout", "rmsnorm", "rmsnorm_ptr", "forward_qk8", "forward_qk8_ptr",
            "rmsnorm_e4m3", "rmsnorm_e4m3_ptr", "forward_ws_ptr", "forward_qk8_ws_ptr",
-           "workspace_size",
+           "workspace_size", "forward_noalloc", "forward_noalloc_ptr",
            "last_cuda_error", "version", "library_path", "DitAttnError", "STATUS",
            "EXPORTED_SYMBOLS"]
 
@@ -42,7 +42,8 @@ EXPORTED_SYMBOLS = ("dit_attn_version", "dit_attn_create", "dit_attn_forward",
                     "dit_attn_destroy", "dit_attn_status_string", "dit_attn_get_device_error",
                     "dit_attn_check_wait_timeout", "dit_attn_last_cuda_error", "dit_attn_rmsnorm",
                     "dit_attn_forward_qk8", "dit_attn_rmsnorm_e4m3", "dit_attn_forward_ws",
-                    "dit_attn_forward_qk8_ws", "dit_attn_workspace_size")
+                    "dit_attn_forward_qk8_ws", "dit_attn_workspace_size",
+                    "dit_attn_forward_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -100,6 +101,9 @@ def _load():
             lib.dit_attn_forward_qk8_ws.argtypes = [vp, vp, vp, vp, c_int, c_int, c_int, c_int,
                                                     c_int, ctypes.c_float, ctypes.c_float,
                                                     ctypes.c_float, vp, ctypes.c_longlong, vp]
+            lib.dit_attn_forward_noalloc.restype = c_int
+            lib.dit_attn_forward_noalloc.argtypes = [vp, vp, vp, vp, c_int, c_int, c_int, c_int,
+                                                     c_int, ctypes.c_float, vp]
             lib.dit_attn_workspace_size.restype = c_int
             lib.dit_attn_workspace_size.argtypes = [c_int, c_int, c_int, c_int, c_int, c_int,
                                                     ctypes.POINTER(ctypes.c_longlong)]
@@ -374,4 +378,31 @@ def rmsnorm_e4m3(x, out_scale: float, weight=None, eps: float = 1e-6, out=None, 
                               _stream_handle(stream))
     if rc:
         raise DitAttnError(rc, "dit_attn_rmsnorm_e4m3")
+    return out
+
+
+def forward_noalloc_ptr(q: int, k: int, v: int, out: int, B: int, H: int, Lq: int, Lk: int, d: int,
+                        scale: float, stream=0) -> int:
+    """Raw C-ABI call of dit_attn_forward_noalloc with integer device pointers."""
+    s = stream if isinstance(stream, ctypes.c_void_p) else ctypes.c_void_p(int(stream))
+    return _load().dit_attn_forward_noalloc(ctypes.c_void_p(q), ctypes.c_void_p(k),
+                                            ctypes.c_void_p(v), ctypes.c_void_p(out), B, H, Lq,
+                                            Lk, d, ctypes.c_float(scale), s)
+
+
+def forward_noalloc(q, k, v, out, scale: float | None = None, stream=None):
+    """forward() with the split tail's scratch held by the library: no memory is
+    allocated by the call (``out`` must be given).  Calls must not overlap."""
+    import torch
+    B, H, Lq, Lk, d = _check_qkv(q, k, v, (torch.bfloat16,))
+    if out is None:
+        raise ValueError("forward_noalloc needs an output tensor")
+    out = _out_like(out, q, (B, H, Lq, d))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    with torch.cuda.device(q.device):
+        rc = forward_noalloc_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                 B, H, Lq, Lk, d, float(scale), _stream_handle(stream))
+    if rc:
+        raise DitAttnError(rc, "dit_attn_forward_noalloc")
     return out

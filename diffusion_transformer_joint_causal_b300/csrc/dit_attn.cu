@@ -1054,6 +1054,35 @@ int dit_attn_forward_qk8(const void* q8, const void* k8, const void* v, void* ou
                                  nullptr, 0, stream);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Scratch of dit_attn_forward_noalloc, a file-scope device array: room for the
+// split tail's partial rows (512 x (128 + 2) fp32 per key-range chunk) of up
+// to kScratchChunks chunks.  A split plan needs at most one chunk per CTA pair
+// (74 on a B300); a larger plan runs unsplit instead.
+constexpr int64_t kScratchChunks = 80;
+constexpr int64_t kScratchBytes =
+    kScratchChunks * kPairUnitRows * (128 + 2) * static_cast<int64_t>(sizeof(float));
+static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
+
+}  // namespace
+
+extern "C" {
+
+int dit_attn_forward_noalloc(const void* q, const void* k, const void* v, void* out, int B, int H,
+                             int Lq, int Lk, int d, float scale, void* stream) {
+  const int rc = check_forward_args(q, k, v, out, B, H, Lq, Lk, d, scale, 2);
+  if (rc != DIT_ATTN_OK) return rc;
+  int dev = -1;
+  if (!current_device(&dev)) return DIT_ATTN_ERR_NO_DEVICE;
+  void* scratch = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&scratch, g_scratch);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return dit_attn_forward_ws(q, k, v, out, B, H, Lq, Lk, d, scale, scratch, kScratchBytes, stream);
+}
+
 int dit_attn_workspace_size(int B, int H, int Lq, int Lk, int d, int qk8, long long* bytes) {
   if (!bytes) return DIT_ATTN_ERR_INVALID_ARG;
   *bytes = 0;

@@ -95,6 +95,18 @@ int dit_attn_forward_ws(const void* q, const void* k, const void* v, void* out, 
                         long long workspace_bytes, void* stream);
 
 /*
+ * dit_attn_forward with the split tail's workspace taken from a scratch array
+ * that the library holds in device memory for its whole lifetime (about 21 MB,
+ * reserved when the library loads): the call itself allocates nothing and
+ * needs no workspace argument.  The scratch is shared by every call on a
+ * device, so calls through this entry point must not overlap in time (one
+ * stream, or ordered streams); a split plan larger than the scratch runs
+ * unsplit.  Arguments, results and errors as dit_attn_forward_ws.
+ */
+int dit_attn_forward_noalloc(const void* q, const void* k, const void* v, void* out, int B, int H,
+                             int Lq, int Lk, int d, float scale, void* stream);
+
+/*
  * Workspace bytes that dit_attn_forward_ws (qk8 = 0) or dit_attn_forward_qk8_ws
  * (qk8 = 1) uses for these sizes on the current device; 0 when no split
  * applies (d = 64, or the last wave is full or its units too short).  Size
