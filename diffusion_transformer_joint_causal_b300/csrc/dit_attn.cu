@@ -776,7 +776,7 @@ cudaLaunchConfig_t pair_launch_config(int grid, cudaStream_t stream, cudaLaunchA
                                       uint32_t smem_bytes = dit::PairTraits::kSmemBytes) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(dit::kNumThreads, 1, 1);
+  cfg.blockDim = dim3(dit::kPairThreads, 1, 1);
   cfg.dynamicSmemBytes = smem_bytes;
   cfg.stream = stream;
   attr->id = cudaLaunchAttributeClusterDimension;

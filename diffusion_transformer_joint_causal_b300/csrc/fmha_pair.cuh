@@ -27,6 +27,20 @@
 
 namespace dit {
 
+// Warp roles of the pair kernel (640 threads, five warpgroups): warps 0-7
+// run the softmax of query tile 0 and warps 8-15 that of tile 1, so the two
+// warps of a tile on an SM sub-partition have two partners working on the
+// other tile while they wait; warp 16 issues the MMAs (leader CTA) and owns
+// TMEM, warp 17 loads, warps 18-19 only complete the fifth warpgroup.
+// Registers: launched at 96 per thread (640 x 96 = 61440); the four softmax
+// warpgroups raise to 112 and the fifth drops to 32: 512 x 112 + 128 x 32 =
+// 61440.
+constexpr int kPairThreads = 640;
+constexpr int kPairMmaWarp = 16;
+constexpr int kPairLoadWarp = 17;
+constexpr int kPairRegsSoftmax = 112;
+constexpr int kPairRegsOther = 32;
+
 template <bool kQK8>
 struct PairTraitsT {
   static constexpr int D = 128;
@@ -284,10 +298,177 @@ __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) 
   __syncwarp();
 }
 
+// ----------------------------------------------------------------- softmax (pair kernel)
+template <bool kMasked>
+__device__ __forceinline__ float rowmax_chunk(const uint32_t (&sr)[32], int key0, int valid) {
+  float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    float a = __uint_as_float(sr[i]), b = __uint_as_float(sr[i + 1]);
+    if (kMasked) {
+      a = (key0 + i < valid) ? a : -INFINITY;
+      b = (key0 + i + 1 < valid) ? b : -INFINITY;
+    }
+    m[(i / 2) & 3] = fmax3(m[(i / 2) & 3], a, b);
+  }
+  return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+}
+
+// One query tile's softmax step for this thread's half-row (keys key0 ..
+// key0+63 of the tile) with a small register footprint: the logits are read
+// from TMEM 32 columns at a time, and the probabilities of both chunks are
+// stored once, at the end, over the half-row's first 32 S columns, so that a
+// recompute can read the logits again.  Otherwise as softmax_tile_half.
+template <int D, class ORescale>
+__device__ __forceinline__ void softmax_tile_lean(uint32_t taddr_s, int key0, bool first,
+                                                  bool masked, int valid, float scale_log2,
+                                                  float& m_used, float& l, ORescale&& o_rescale) {
+  uint32_t sr[32];
+  uint32_t pk[32];
+  float acc[8];
+  auto load = [&](int c) {
+    tmem_ld16x2_32<64>(taddr_s + 32 * c, sr);
+    tmem_wait_ld();
+  };
+  auto probs = [&](int c, float m) {
+    if (masked) probs_chunk<true>(sr, scale_log2, -m, key0 + 32 * c, valid, &pk[16 * c], acc);
+    else probs_chunk<false>(sr, scale_log2, -m, key0 + 32 * c, kBN, &pk[16 * c], acc);
+  };
+  auto chunk_max = [&](int c) -> float {
+    return masked ? rowmax_chunk<true>(sr, key0 + 32 * c, valid)
+                  : rowmax_chunk<false>(sr, key0 + 32 * c, kBN);
+  };
+  auto clear = [&]() {
+#pragma unroll
+    for (int a = 0; a < 8; ++a) acc[a] = 0.f;
+  };
+  // Row max over both halves, lazy rescale of l and O, then the probabilities
+  // (sr holds chunk 1 after the max, so it goes first).
+  auto max_pass = [&]() {
+    load(0);
+    float mx = chunk_max(0);
+    load(1);
+    mx = fmaxf(mx, chunk_max(1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    const float m_tile = mx * scale_log2;
+    float factor = 1.f;
+    if (m_tile > m_used + kRescaleThreshold) {
+      factor = ex2_approx(m_used - m_tile);   // 0 on the first tile
+      l *= factor;
+      m_used = m_tile;
+    }
+    if (!first && __any_sync(0xffffffffu, factor != 1.f)) o_rescale(factor);
+    clear();
+    probs(1, m_used);
+    load(0);
+    probs(0, m_used);
+  };
+  clear();
+  if (first) {
+    max_pass();
+  } else {
+    // Optimistic pass against the running max; a rounded row sum above 2^16
+    // means some p > 2^9: raise the max (always by more than 8), rescale l
+    // and O, recompute.  Warp-uniform branch.
+    load(0);
+    probs(0, m_used);
+    load(1);
+    probs(1, m_used);
+    const float half_sum = sum8(acc);
+    const float row_sum = half_sum + __shfl_xor_sync(0xffffffffu, half_sum, 16);
+    if (__any_sync(0xffffffffu, !(row_sum <= kOptimisticSumLimit))) max_pass();
+  }
+  tmem_st16x2_16<64>(taddr_s, &pk[0]);
+  tmem_st16x2_16<64>(taddr_s + 16, &pk[16]);
+  l += sum8(acc);
+}
+
+// Softmax and epilogue of the pair kernel: warp w works on query tile w / 8,
+// TMEM lanes 32*(w%4) + 16*((w/8)... two threads per row as in softmax_role.
+// Each warp arrives once per key tile on its tile's P-ready barrier of the
+// leader CTA (8 warps x 2 CTAs).
+template <int D, class T>
+__device__ void softmax_role_pair(const Params& p, const Shared& sh, uint32_t tmem) {
+  const int warp = threadIdx.x / 32;                 // 0..15
+  const int lane = threadIdx.x & 31;
+  const int t = warp >> 3;                           // query tile
+  const int wq = warp & 7;
+  const int half = lane >> 4;                        // keys [64*half, 64*half + 64) of a tile
+  const int lane0 = (wq & 3) * 32 + (wq >> 2) * 16;  // warp % 4 == wq % 4: its TMEM sub-partition
+  const int r = lane0 + (lane & 15);                 // row within the query tile
+  const uint32_t lane_addr = tmem + (static_cast<uint32_t>(lane0) << 16);
+  const uint32_t taddr_s = lane_addr + T::col_s(t);
+  const uint32_t taddr_o = lane_addr + T::col_o(t);
+  const float scale_log2 = p.scale_log2;
+  const int n_kv = (p.Lk + kBN - 1) / kBN;
+  const int tail = p.Lk - (n_kv - 1) * kBN;          // valid keys in the last tile, 1..128
+  const int key0 = 64 * half;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const uint32_t p_full_leader = mapa_shared(sh.bar(T::kBarPFull + t), 0);
+  uint32_t g = 0, it = 0;
+  bool ok = true;
+
+  for (int i = static_cast<int>(cluster_id_x()); i < p.num_items && ok;
+       i += static_cast<int>(num_clusters_x()), ++it) {
+    const WorkItem w = work_item(i, p, n_kv);
+    float m_used = -INFINITY;   // running max, in units of s*scale*log2(e)
+    float l = 0.f;              // this half-row's share of the row sum
+    for (int j = w.j0; j < w.j1 && ok; ++j, ++g) {
+      const bool masked = (j == n_kv - 1) && (tail < kBN);
+      const int valid = masked ? tail : kBN;
+      const bool got = mbar_wait(sh.bar(T::kBarSFull + t), g & 1u, kWaitLimitNs, sh.abort);
+      if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+      tc_fence_after();
+      // O_t is quiescent here: S_t's completion implies the previous P.V
+      // product into O_t finished.
+      softmax_tile_lean<D>(taddr_s, key0, j == w.j0, masked, valid, scale_log2, m_used, l,
+                           [&](float f) { rescale_o_half<D>(taddr_o, f); });
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(p_full_leader);
+    }
+    if (!ok) break;
+    // Epilogue: O_t / l -> bf16 -> global, each thread its D/2 columns; a
+    // chunk of a split unit stores O_t, its max and row sum unnormalised.
+    const bool got = mbar_wait(sh.bar(T::kBarOFull + t), it & 1u, kWaitLimitNs, sh.abort);
+    if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+    tc_fence_after();
+    const float l_row = l + __shfl_xor_sync(0xffffffffu, l, 16);
+    const int prow = rank * kUnitRows + t * kBM + r;   // row within the 512-row unit
+    if (w.chunk >= 0) {
+      store_partial<D>(p, static_cast<int64_t>(w.chunk) * (2 * kUnitRows) + prow, half, taddr_o,
+                       m_used, l_row);
+      continue;
+    }
+    const float inv_l = 1.f / l_row;
+    const int row = w.qblock * (2 * kUnitRows) + prow;
+    const bool row_ok = row < p.Lq;
+    uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(w.bh) * p.Lq + row) * D +
+                                          half * (D / 2));
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c) {
+      uint32_t o[32];
+      tmem_ld16x2_32<D / 2>(taddr_o + c * 32, o);
+      tmem_wait_ld();
+      uint32_t wv[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        wv[k] = pack_bf16x2(__uint_as_float(o[2 * k]) * inv_l, __uint_as_float(o[2 * k + 1]) * inv_l);
+      if (row_ok) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          dst[c * 4 + v] = make_uint4(wv[4 * v], wv[4 * v + 1], wv[4 * v + 2], wv[4 * v + 3]);
+      }
+    }
+  }
+  if (!ok) record_timeout<true>(sh);
+}
+
 // ----------------------------------------------------------------- kernel
 // Launched with a cluster dimension of 2 (consecutive CTAs form a pair).
 template <bool kQK8>
-__global__ void __launch_bounds__(kNumThreads, 1)
+__global__ void __launch_bounds__(kPairThreads, 1)
     fmha_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const Params p) {
@@ -321,12 +502,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     *sh.abort = 0;
     fence_mbarrier_init();
   }
-  if (warp == kLoadWarp && lane == 0) {
+  if (warp == kPairLoadWarp && lane == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
   }
-  if (warp == kMmaWarp) {
+  if (warp == kPairMmaWarp) {
     tmem_alloc_pair(smem_u32(misc), T::kTmemCols);
     tmem_relinquish_pair();
   }
@@ -337,18 +518,18 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   tc_fence_after();
   const uint32_t tmem = misc[0];
 
-  if (warp < kMmaWarp) {
-    reg_alloc<kRegsSoftmax>();
-    softmax_role<T::D, T, true>(p, sh, tmem);
-  } else if (warp == kMmaWarp) {
-    reg_dealloc<kRegsOther>();
+  if (warp < kPairMmaWarp) {
+    reg_alloc<kPairRegsSoftmax>();
+    softmax_role_pair<T::D, T>(p, sh, tmem);
+  } else if (warp == kPairMmaWarp) {
+    reg_dealloc<kPairRegsOther>();
     if (leader) pair_mma_role<kQK8>(p, sh, tmem);
-  } else if (warp == kLoadWarp) {
-    reg_dealloc<kRegsOther>();
+  } else if (warp == kPairLoadWarp) {
+    reg_dealloc<kPairRegsOther>();
     if (lane == 0) pair_load_role<kQK8>(&tmQ, &tmK, &tmV, p, sh);
     __syncwarp();
   } else {
-    reg_dealloc<kRegsOther>();
+    reg_dealloc<kPairRegsOther>();
   }
 
   // The leader drained its MMAs; neither CTA leaves while the pair's MMAs or
@@ -356,7 +537,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();
-  if (warp == kMmaWarp) {
+  if (warp == kPairMmaWarp) {
     tc_fence_after();
     tmem_dealloc_pair(tmem, T::kTmemCols);
   }
