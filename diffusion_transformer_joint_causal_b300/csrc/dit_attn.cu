@@ -498,11 +498,10 @@ __device__ __forceinline__ void store_partial(const Params& p, int64_t prow, int
   if (half == 0) reinterpret_cast<float2*>(p.part_ml)[prow] = make_float2(m_used, l_row);
 }
 
-// kPair: the CTA is one half of a pair; a work unit then spans 512 query rows
-// (this CTA's 256 start at rank*256) and P-ready is reported on the barrier of
-// the pair's leader CTA, whose warp issues the MMAs.  Each warp arrives once
-// per tile (after its TMEM stores completed).
-template <int D, class T, bool kPair>
+// Softmax and epilogue of the single-CTA kernel: the eight softmax warps take
+// query tile 0, then tile 1, of every key tile; each warp arrives once per
+// tile on P-ready (after its TMEM stores completed).
+template <int D, class T>
 __device__ void softmax_role(const Params& p, const Shared& sh, uint32_t tmem) {
   const int warp = threadIdx.x / 32;                 // 0..7
   const int lane = threadIdx.x & 31;
@@ -516,19 +515,14 @@ __device__ void softmax_role(const Params& p, const Shared& sh, uint32_t tmem) {
   const int key0 = 64 * half;
   uint32_t g = 0, it = 0;
   bool ok = true;
-  const int rank = kPair ? static_cast<int>(cluster_ctarank()) : 0;
-  const int u0 = kPair ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
-  const int u_stride = kPair ? static_cast<int>(num_clusters_x()) : static_cast<int>(gridDim.x);
-  const int unit_rows = kPair ? 2 * kUnitRows : kUnitRows;
-  const uint32_t p_full_leader0 = kPair ? mapa_shared(sh.bar(T::kBarPFull), 0) : 0u;
 
-  for (int i = u0; i < p.num_items && ok; i += u_stride, ++it) {
-    const WorkItem w = work_item(i, p, n_kv);
-    const int bh = w.bh;
-    const int row_base = w.qblock * unit_rows + rank * kUnitRows + r;
+  for (int u = static_cast<int>(blockIdx.x); u < p.num_units && ok;
+       u += static_cast<int>(gridDim.x), ++it) {
+    const int bh = u / p.num_qblocks;
+    const int row_base = (u % p.num_qblocks) * kUnitRows + r;
     float m_used[2] = {-INFINITY, -INFINITY};   // running max, in units of s*scale*log2(e)
     float l[2] = {0.f, 0.f};                     // this half-row's share of the row sum
-    for (int j = w.j0; j < w.j1 && ok; ++j, ++g) {
+    for (int j = 0; j < n_kv && ok; ++j, ++g) {
       const bool masked = (j == n_kv - 1) && (tail < kBN);
       const int valid = masked ? tail : kBN;
 #pragma unroll
@@ -539,32 +533,22 @@ __device__ void softmax_role(const Params& p, const Shared& sh, uint32_t tmem) {
         // O_t is quiescent here: S_t's completion implies the previous P.V
         // product into O_t finished.
         const uint32_t taddr_o = lane_addr + T::col_o(t);
-        softmax_tile_half<D>(lane_addr + T::col_s(t), key0, j == w.j0, masked, valid, scale_log2,
+        softmax_tile_half<D>(lane_addr + T::col_s(t), key0, j == 0, masked, valid, scale_log2,
                              m_used[t], l[t], [&](float f) { rescale_o_half<D>(taddr_o, f); });
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          if (kPair) mbar_arrive_cluster(p_full_leader0 + 8u * t);
-          else mbar_arrive(sh.bar(T::kBarPFull + t));
-        }
+        if (lane == 0) mbar_arrive(sh.bar(T::kBarPFull + t));
       }
     }
     if (!ok) break;
     // Epilogue: O_t / l -> bf16 -> global; each thread writes its D/2 columns.
-    // A chunk of a split unit stores O_t, its max and row sum unnormalised.
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       const bool got = mbar_wait(sh.bar(T::kBarOFull + t), it & 1u, kWaitLimitNs, sh.abort);
       if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
       tc_fence_after();
       const float l_row = l[t] + __shfl_xor_sync(0xffffffffu, l[t], 16);
-      if (kPair && w.chunk >= 0) {
-        const int64_t prow = static_cast<int64_t>(w.chunk) * (2 * kUnitRows) + rank * kUnitRows +
-                             t * kBM + r;
-        store_partial<D>(p, prow, half, lane_addr + T::col_o(t), m_used[t], l_row);
-        continue;
-      }
       const float inv_l = 1.f / l_row;
       const int row = row_base + t * kBM;
       const bool row_ok = row < p.Lq;
@@ -576,19 +560,19 @@ __device__ void softmax_role(const Params& p, const Shared& sh, uint32_t tmem) {
         uint32_t o[32];
         tmem_ld16x2_32<D / 2>(taddr_o + c * 32, o);
         tmem_wait_ld();
-        uint32_t w[16];
+        uint32_t wv[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+          wv[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
         if (row_ok) {
 #pragma unroll
           for (int v = 0; v < 4; ++v)
-            dst[c * 4 + v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+            dst[c * 4 + v] = make_uint4(wv[4 * v], wv[4 * v + 1], wv[4 * v + 2], wv[4 * v + 3]);
         }
       }
     }
   }
-  if (!ok) record_timeout<kPair>(sh);
+  if (!ok) record_timeout(sh);
 }
 
 // ----------------------------------------------------------------- kernel
@@ -641,7 +625,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
   if (warp < kMmaWarp) {
     reg_alloc<kRegsSoftmax>();
-    softmax_role<D, Traits<D>, false>(p, sh, tmem);
+    softmax_role<D, Traits<D>>(p, sh, tmem);
   } else if (warp == kMmaWarp) {
     reg_dealloc<kRegsOther>();
     mma_role<D>(p, sh, tmem);
