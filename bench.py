@@ -296,6 +296,9 @@ def cpu_baseline(w, seconds: float):
 
 def bench_reference(args):
     import workloads as W
+    if args.path != "bf16":
+        raise SystemExit("--impl reference times the FP64 oracle on the bf16 inputs; "
+                         "it takes no --path")
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
@@ -322,8 +325,9 @@ def bench_reference(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "Lq": w.Lq, "Lk": w.Lk, "d": w.d,
-                   "rows_per_step": per_step},
+        "config": {"workload": w.name, "path": args.path, "B": w.B, "H": w.H, "Lq": w.Lq,
+                   "Lk": w.Lk, "d": w.d, "segments": dict(w.segments),
+                   "parallelism": f"replicas x{args.gpus}", "rows_per_step": per_step},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": f"{per_step} query rows of {w.name} per step, FP64 C loop"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
