@@ -250,3 +250,38 @@ def test_split_tail_short_workspace_runs_unsplit(dit):
     b = dit.forward(q, k, v, 0.088, workspace=None)
     torch.cuda.synchronize()
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_repeated_calls_bit_identical_at_scale(dit):
+    # The full 2048x2048 text-to-image workload (split last wave included):
+    # every call of a run, and calls on a second stream, give the same bits.
+    import torch
+    w = W.workload("2048px_t2i_cfg")
+    q, k, v = (to_device(x) for x in W.make_qkv(w))
+    first = dit.forward(q, k, v, w.scale)
+    outs = [dit.forward(q, k, v, w.scale) for _ in range(4)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        outs.append(dit.forward(q, k, v, w.scale))
+    torch.cuda.synchronize()
+    for o in outs:
+        assert torch.equal(o.view(torch.int16), first.view(torch.int16))
+
+
+def test_many_heads_short_rows(dit):
+    # 160 (b,h) pairs of 300 queries against 2100 keys: 160 work units on 74
+    # CTA pairs, the last wave's 12 units split in two key ranges, ragged
+    # query and key tails.
+    B, H, Lq, Lk, d = 2, 80, 300, 2100, 128
+    assert dit.workspace_size(B, H, Lq, Lk, d) > 0
+    rng = np.random.default_rng(2300)
+    q = W.random_bf16(rng, (B, H, Lq, d))
+    k = W.random_bf16(rng, (B, H, Lk, d))
+    v = W.random_bf16(rng, (B, H, Lk, d))
+    scale = float(np.float32(1 / math.sqrt(d)))
+    got = to_host_f64(run(dit, q, k, v, scale))
+    bh = np.repeat(np.arange(B * H), 8)
+    rows = np.tile(np.array([0, 1, 127, 128, 255, 256, 298, 299]), B * H)
+    flat = got.reshape(B * H, Lq, d)[bh, rows]
+    assert_close(flat, oracle_sampled(q, k, v, scale, bh, rows), "many heads")
