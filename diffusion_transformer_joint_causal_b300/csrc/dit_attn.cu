@@ -48,10 +48,13 @@ constexpr int kBM = 128;                 // query rows per tile (one TMEM lane e
 constexpr int kBN = 128;                 // keys per K/V tile
 constexpr int kTilesPerUnit = 2;         // query tiles per work unit
 constexpr int kUnitRows = kBM * kTilesPerUnit;
-constexpr int kNumThreads = 384;       // three full warpgroups (setmaxnreg works per warpgroup)
-// Register split: launched at 168 per thread (384 x 168 = 64512); the two
-// softmax warpgroups raise to 208 and the MMA/TMA warpgroup drops to 88:
-// 256 x 208 + 128 x 88 = 64512, exactly the launch's total.
+// The single-CTA kernel (d = 64) runs three full warpgroups (setmaxnreg
+// works per warpgroup); the d = 128 CTA-pair kernel has its own constants.
+constexpr int kNumThreads = 384;
+// Register split of the single-CTA kernel: launched at 168 per thread
+// (384 x 168 = 64512); the two softmax warpgroups raise to 208 and the
+// MMA/TMA warpgroup drops to 88: 256 x 208 + 128 x 88 = 64512, exactly the
+// launch's total.
 constexpr int kRegsSoftmax = 208;
 constexpr int kRegsOther = 88;
 constexpr int kMmaWarp = 8;
@@ -342,10 +345,10 @@ __device__ void mma_role(const Params& p, const Shared& sh, uint32_t tmem) {
 }
 
 // ----------------------------------------------------------------- softmax + epilogue
-// The eight softmax warps work on one query tile at a time, two threads per
-// query row (TMEM shape 16x32bx2): warp w owns TMEM lanes 32*(w%4) + 16*(w/4)
-// .. +15; lanes 0-15 of the warp take keys 0-63 of the tile and lanes 16-31
-// take keys 64-127 of the same rows.  A half-row's probabilities (32 packed
+// Single-CTA kernel (d = 64): the eight softmax warps work on one query tile
+// at a time, two threads per query row (TMEM shape 16x32bx2): warp w owns
+// TMEM lanes 32*(w%4) + 16*(w/4) .. +15; lanes 0-15 of the warp take keys
+// 0-63 of the tile and lanes 16-31 take keys 64-127 of the same rows.  A half-row's probabilities (32 packed
 // bf16 pairs) go over the first 32 columns of its own 64 S columns, so the two
 // halves never overwrite each other's logits.  Row max, row sum and the
 // recompute decision are combined across the pair with one shuffle.
