@@ -15,6 +15,11 @@ fallback: if the library is missing, importing the names below raises.
     q8 = dit.rmsnorm_e4m3(q, out_scale=1 / s)
     k8 = dit.rmsnorm_e4m3(k, out_scale=1 / s)
     out = dit.forward_qk8(q8, k8, v, q_scale=s, k_scale=s)
+
+    # e4m3 values too (P rounded to e4m3 before P.V); v_scale from calibration
+    v_scale = float(v.abs().max()) / 448
+    v8 = dit.quantize_e4m3(v, out_scale=1 / v_scale)
+    out = dit.forward_fp8(q8, k8, v8, q_scale=s, k_scale=s, v_scale=v_scale)
 """
 from __future__ import annotations
 
@@ -26,7 +31,8 @@ import threading
 __all__ = ["create", "destroy", "forward", "forward_ptr", "status_string", "get_device_error",
            "check_wait_timeout", "rmsnorm", "rmsnorm_ptr", "forward_qk8", "forward_qk8_ptr",
            "rmsnorm_e4m3", "rmsnorm_e4m3_ptr", "forward_ws_ptr", "forward_qk8_ws_ptr",
-           "workspace_size", "forward_noalloc", "forward_noalloc_ptr",
+           "workspace_size", "forward_noalloc", "forward_noalloc_ptr", "forward_fp8",
+           "forward_fp8_ptr", "forward_fp8_ws_ptr", "quantize_e4m3", "quantize_e4m3_ptr",
            "last_cuda_error", "version", "library_path", "DitAttnError", "STATUS",
            "EXPORTED_SYMBOLS"]
 
@@ -43,7 +49,8 @@ EXPORTED_SYMBOLS = ("dit_attn_version", "dit_attn_create", "dit_attn_forward",
                     "dit_attn_check_wait_timeout", "dit_attn_last_cuda_error", "dit_attn_rmsnorm",
                     "dit_attn_forward_qk8", "dit_attn_rmsnorm_e4m3", "dit_attn_forward_ws",
                     "dit_attn_forward_qk8_ws", "dit_attn_workspace_size",
-                    "dit_attn_forward_noalloc")
+                    "dit_attn_forward_noalloc", "dit_attn_forward_fp8",
+                    "dit_attn_forward_fp8_ws", "dit_attn_quantize_e4m3")
 
 _lock = threading.Lock()
 _lib = None
@@ -107,6 +114,17 @@ def _load():
             lib.dit_attn_workspace_size.restype = c_int
             lib.dit_attn_workspace_size.argtypes = [c_int, c_int, c_int, c_int, c_int, c_int,
                                                     ctypes.POINTER(ctypes.c_longlong)]
+            lib.dit_attn_forward_fp8.restype = c_int
+            lib.dit_attn_forward_fp8.argtypes = [vp, vp, vp, vp, c_int, c_int, c_int, c_int, c_int,
+                                                 ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                                 ctypes.c_float, vp]
+            lib.dit_attn_forward_fp8_ws.restype = c_int
+            lib.dit_attn_forward_fp8_ws.argtypes = [vp, vp, vp, vp, c_int, c_int, c_int, c_int,
+                                                    c_int, ctypes.c_float, ctypes.c_float,
+                                                    ctypes.c_float, ctypes.c_float, vp,
+                                                    ctypes.c_longlong, vp]
+            lib.dit_attn_quantize_e4m3.restype = c_int
+            lib.dit_attn_quantize_e4m3.argtypes = [vp, vp, ctypes.c_longlong, ctypes.c_float, vp]
             lib.dit_attn_last_cuda_error.restype = c_int
             lib.dit_attn_last_cuda_error.argtypes = []
             _lib = lib
@@ -165,9 +183,10 @@ def forward_ptr(q: int, k: int, v: int, out: int, B: int, H: int, Lq: int, Lk: i
                                     ctypes.c_float(scale), s)
 
 
-def _check_qkv(q, k, v, qk_dtypes):
+def _check_qkv(q, k, v, qk_dtypes, v_dtypes=None):
     import torch
-    for name, t, dtypes in (("q", q, qk_dtypes), ("k", k, qk_dtypes), ("v", v, (torch.bfloat16,))):
+    v_dtypes = v_dtypes or (torch.bfloat16,)
+    for name, t, dtypes in (("q", q, qk_dtypes), ("k", k, qk_dtypes), ("v", v, v_dtypes)):
         if not isinstance(t, torch.Tensor) or t.dtype not in dtypes or not t.is_cuda:
             raise TypeError(f"{name} must be a CUDA tensor of dtype {' or '.join(map(str, dtypes))}")
         if t.dim() != 4 or not t.is_contiguous():
@@ -191,19 +210,23 @@ def _out_like(out, q, shape):
     return out
 
 
-def workspace_size(B: int, H: int, Lq: int, Lk: int, d: int, qk8: bool = False) -> int:
-    """Bytes of split-tail workspace the forward uses for these sizes (0: none)."""
+def workspace_size(B: int, H: int, Lq: int, Lk: int, d: int, qk8: bool = False,
+                   variant: int | None = None) -> int:
+    """Bytes of split-tail workspace the forward uses for these sizes (0: none).
+    variant: 0 forward, 1 forward_qk8, 2 forward_fp8 (default: 1 if qk8 else 0)."""
+    if variant is None:
+        variant = 1 if qk8 else 0
     nb = ctypes.c_longlong(0)
-    rc = _load().dit_attn_workspace_size(B, H, Lq, Lk, d, int(bool(qk8)), ctypes.byref(nb))
+    rc = _load().dit_attn_workspace_size(B, H, Lq, Lk, d, int(variant), ctypes.byref(nb))
     if rc:
         raise DitAttnError(rc, "dit_attn_workspace_size")
     return nb.value
 
 
-_ws_sizes = {}   # (device index, sizes, qk8) -> workspace bytes; fixed once a device is created
+_ws_sizes = {}   # (device index, sizes, variant) -> workspace bytes; fixed once a device is created
 
 
-def _workspace(workspace, device, B, H, Lq, Lk, d, qk8, stream):
+def _workspace(workspace, device, B, H, Lq, Lk, d, variant, stream):
     """(tensor, pointer, bytes) of the workspace: "auto" allocates what the
     library asks for through torch's caching allocator, ordered on the stream
     the call runs on; None runs unsplit; a uint8 CUDA tensor is used as given."""
@@ -213,10 +236,10 @@ def _workspace(workspace, device, B, H, Lq, Lk, d, qk8, stream):
     if isinstance(workspace, str):
         if workspace != "auto":
             raise ValueError('workspace must be "auto", None or a uint8 CUDA tensor')
-        key = (device.index, B, H, Lq, Lk, d, bool(qk8))
+        key = (device.index, B, H, Lq, Lk, d, int(variant))
         nb = _ws_sizes.get(key)
         if nb is None:   # the caller has made `device` current
-            nb = 0 if d == 64 else workspace_size(B, H, Lq, Lk, d, qk8)
+            nb = 0 if d == 64 else workspace_size(B, H, Lq, Lk, d, variant=int(variant))
             _ws_sizes[key] = nb
         if nb == 0:
             return None, 0, 0
@@ -256,7 +279,7 @@ def forward(q, k, v, scale: float | None = None, out=None, stream=None, workspac
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     with torch.cuda.device(q.device):
-        ws, ws_ptr, ws_bytes = _workspace(workspace, q.device, B, H, Lq, Lk, d, False, stream)
+        ws, ws_ptr, ws_bytes = _workspace(workspace, q.device, B, H, Lq, Lk, d, 0, stream)
         rc = forward_ws_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                             B, H, Lq, Lk, d, float(scale), ws_ptr, ws_bytes,
                             _stream_handle(stream))
@@ -334,7 +357,7 @@ def forward_qk8(q8, k8, v, q_scale: float, k_scale: float, scale: float | None =
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     with torch.cuda.device(v.device):
-        ws, ws_ptr, ws_bytes = _workspace(workspace, v.device, B, H, Lq, Lk, d, True, stream)
+        ws, ws_ptr, ws_bytes = _workspace(workspace, v.device, B, H, Lq, Lk, d, 1, stream)
         rc = forward_qk8_ws_ptr(q8.data_ptr(), k8.data_ptr(), v.data_ptr(), out.data_ptr(),
                                 B, H, Lq, Lk, d, float(scale), float(q_scale), float(k_scale),
                                 ws_ptr, ws_bytes, _stream_handle(stream))
@@ -405,4 +428,81 @@ def forward_noalloc(q, k, v, out, scale: float | None = None, stream=None):
                                  B, H, Lq, Lk, d, float(scale), _stream_handle(stream))
     if rc:
         raise DitAttnError(rc, "dit_attn_forward_noalloc")
+    return out
+
+
+def forward_fp8_ptr(q8: int, k8: int, v8: int, out: int, B: int, H: int, Lq: int, Lk: int, d: int,
+                    scale: float, q_scale: float, k_scale: float, v_scale: float, stream=0) -> int:
+    """Raw C-ABI call of dit_attn_forward_fp8 with integer device pointers; returns the status."""
+    s = stream if isinstance(stream, ctypes.c_void_p) else ctypes.c_void_p(int(stream))
+    return _load().dit_attn_forward_fp8(ctypes.c_void_p(q8), ctypes.c_void_p(k8),
+                                        ctypes.c_void_p(v8), ctypes.c_void_p(out), B, H, Lq, Lk,
+                                        d, ctypes.c_float(scale), ctypes.c_float(q_scale),
+                                        ctypes.c_float(k_scale), ctypes.c_float(v_scale), s)
+
+
+def forward_fp8_ws_ptr(q8: int, k8: int, v8: int, out: int, B: int, H: int, Lq: int, Lk: int,
+                       d: int, scale: float, q_scale: float, k_scale: float, v_scale: float,
+                       workspace: int, workspace_bytes: int, stream=0) -> int:
+    """Raw C-ABI call of dit_attn_forward_fp8_ws with integer device pointers."""
+    s = stream if isinstance(stream, ctypes.c_void_p) else ctypes.c_void_p(int(stream))
+    return _load().dit_attn_forward_fp8_ws(ctypes.c_void_p(q8), ctypes.c_void_p(k8),
+                                           ctypes.c_void_p(v8), ctypes.c_void_p(out), B, H, Lq,
+                                           Lk, d, ctypes.c_float(scale), ctypes.c_float(q_scale),
+                                           ctypes.c_float(k_scale), ctypes.c_float(v_scale),
+                                           ctypes.c_void_p(workspace),
+                                           ctypes.c_longlong(workspace_bytes), s)
+
+
+def forward_fp8(q8, k8, v8, q_scale: float, k_scale: float, v_scale: float,
+                scale: float | None = None, out=None, stream=None, workspace="auto"):
+    """out = v_scale * softmax((q_scale*q8)(k_scale*k8)^T * scale) v8, all three e4m3,
+    with the probabilities rounded to e4m3 before the product with v8.
+
+    q8: [B, H, Lq, 128], k8 and v8: [B, H, Lk, 128], contiguous CUDA tensors of
+    e4m3 codes (torch.float8_e4m3fn or uint8).  scale defaults to 1/sqrt(d);
+    ``workspace`` as for forward.  Returns the bf16 output ``out``.
+    """
+    import torch
+    e4m3 = (torch.float8_e4m3fn, torch.uint8)
+    B, H, Lq, Lk, d = _check_qkv(q8, k8, v8, e4m3, e4m3)
+    out = _out_like(out, v8, (B, H, Lq, d))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    with torch.cuda.device(v8.device):
+        ws, ws_ptr, ws_bytes = _workspace(workspace, v8.device, B, H, Lq, Lk, d, 2, stream)
+        rc = forward_fp8_ws_ptr(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), out.data_ptr(),
+                                B, H, Lq, Lk, d, float(scale), float(q_scale), float(k_scale),
+                                float(v_scale), ws_ptr, ws_bytes, _stream_handle(stream))
+    if rc:
+        raise DitAttnError(rc, "dit_attn_forward_fp8_ws")
+    return out
+
+
+def quantize_e4m3_ptr(x: int, y8: int, n: int, out_scale: float, stream=0) -> int:
+    """Raw C-ABI call of dit_attn_quantize_e4m3 with integer device pointers; returns the status."""
+    s = stream if isinstance(stream, ctypes.c_void_p) else ctypes.c_void_p(int(stream))
+    return _load().dit_attn_quantize_e4m3(ctypes.c_void_p(x), ctypes.c_void_p(y8),
+                                          ctypes.c_longlong(n), ctypes.c_float(out_scale), s)
+
+
+def quantize_e4m3(x, out_scale: float, out=None, stream=None):
+    """out = e4m3(x * out_scale) (fp32 product, nearest even, saturating at 448) for a
+    contiguous bf16 CUDA tensor; returns a torch.float8_e4m3fn tensor shaped like x
+    (or fills ``out``).  The dequantisation scale to hand the forward is 1/out_scale."""
+    import torch
+    if not isinstance(x, torch.Tensor) or x.dtype != torch.bfloat16 or not x.is_cuda:
+        raise TypeError("x must be a bfloat16 CUDA tensor")
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.float8_e4m3fn, device=x.device)
+    elif (out.dtype not in (torch.float8_e4m3fn, torch.uint8) or out.shape != x.shape
+          or not out.is_contiguous() or out.device != x.device):
+        raise ValueError("out must be a contiguous e4m3 (or uint8) tensor shaped like x")
+    with torch.cuda.device(x.device):
+        rc = quantize_e4m3_ptr(x.data_ptr(), out.data_ptr(), x.numel(), float(out_scale),
+                               _stream_handle(stream))
+    if rc:
+        raise DitAttnError(rc, "dit_attn_quantize_e4m3")
     return out

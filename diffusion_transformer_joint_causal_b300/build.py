@@ -13,6 +13,7 @@ CSRC = os.path.join(PKG, "csrc")
 SOURCES = [os.path.join(CSRC, "dit_attn.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "fmha_pair.cuh"),
                   os.path.join(CSRC, "rmsnorm.cuh"), os.path.join(CSRC, "combine.cuh"),
+                  os.path.join(CSRC, "quantize.cuh"),
                   os.path.join(os.path.dirname(PKG), "include", "dit_attn.h")]
 LIB = os.path.join(PKG, "libdit_attn.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")

@@ -108,6 +108,8 @@ struct Params {
   int num_items;     // split_base + (num_units - split_base) * splits
   float* part_o;     // [chunk][512 rows][D] fp32: sum_j p_j v_j against the chunk's max
   float* part_ml;    // [chunk][512 rows][2] fp32: running max (log2 units), row sum
+  float v_scale;     // e4m3 values: dequantisation scale of v (1 otherwise)
+  float inv_v_scale; // 1 / v_scale
 };
 
 // One work item: query block `qblock` of head `bh` against key tiles
@@ -669,6 +671,7 @@ __global__ void wait_timeout_kernel(uint64_t limit_ns) {
 #include "fmha_pair.cuh"
 #include "combine.cuh"
 #include "rmsnorm.cuh"
+#include "quantize.cuh"
 
 // =================================================================== host side
 namespace {
@@ -680,6 +683,7 @@ struct DeviceState {
   int num_sms = 0;
   int max_pairs = 0;       // co-resident clusters of two CTAs of the bf16 pair kernel
   int max_pairs_qk8 = 0;   // the same for the e4m3-QK pair kernel
+  int max_pairs_fp8 = 0;   // the same for the e4m3 Q/K/V pair kernel
 };
 
 constexpr int kMaxDevices = 64;
@@ -702,23 +706,25 @@ bool current_device(int* dev) {
 }
 
 // 3-D view [BH][L][d] of bf16 (elem_bytes 2) or e4m3 bytes (elem_bytes 1)
-// with a box of one 128-byte row segment x box_rows rows and 128-byte
-// swizzle.  Rows beyond L inside one head read as zeros, never as the next
-// head's rows.
+// with a box of one row segment of box_bytes (128 or 64) x box_rows rows,
+// swizzled at the segment's width.  Rows beyond L inside one head read as
+// zeros, never as the next head's rows.
 int encode_map(CUtensorMap* map, const void* ptr, int64_t BH, int64_t L, int d,
-               uint32_t box_rows = 128, int elem_bytes = 2) {
+               uint32_t box_rows = 128, int elem_bytes = 2, uint32_t box_bytes = 128) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(L),
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t eb = static_cast<cuuint64_t>(elem_bytes);
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * eb,
                                  static_cast<cuuint64_t>(L) * static_cast<cuuint64_t>(d) * eb};
-  const cuuint32_t box[3] = {128u / static_cast<cuuint32_t>(elem_bytes), box_rows, 1};
+  const cuuint32_t box[3] = {box_bytes / static_cast<cuuint32_t>(elem_bytes), box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapDataType dtype =
       elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   const CUresult r = g_encode(map, dtype, 3, const_cast<void*>(ptr), dims,
                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              box_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                              : CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     g_last_cuda_error = static_cast<int>(r);
@@ -752,6 +758,8 @@ int launch(const void* q, const void* k, const void* v, void* out, int64_t BH, i
   p.num_items = p.num_units;
   p.part_o = nullptr;
   p.part_ml = nullptr;
+  p.v_scale = 1.f;
+  p.inv_v_scale = 1.f;
   const int grid = p.num_units < num_sms ? p.num_units : num_sms;
   dit::fmha_fwd_kernel<D><<<grid, dit::kNumThreads, Traits<D>::kSmemBytes, stream>>>(tq, tk, tv, p);
   const cudaError_t e = cudaGetLastError();
@@ -808,17 +816,22 @@ SplitPlan plan_split(int64_t num_units, int n_kv, int max_pairs) {
 
 // d = 128: clusters of two CTAs, one work unit = 512 query rows.  With kQK8,
 // q and k hold e4m3 bytes and `scale` already includes their dequantisation
-// scales.  With a workspace of at least the plan's size the last, partial wave
-// runs split, followed by the combine kernel on the same stream.
-template <bool kQK8>
+// scales; with kPV8, v holds e4m3 bytes too, dequantised by v_scale.  With a
+// workspace of at least the plan's size the last, partial wave runs split,
+// followed by the combine kernel on the same stream.
+template <bool kQK8, bool kPV8>
 int launch_pair(const void* q, const void* k, const void* v, void* out, int64_t BH, int Lq, int Lk,
-                double scale, cudaStream_t stream, int max_pairs, void* ws, int64_t ws_bytes) {
+                double scale, cudaStream_t stream, int max_pairs, void* ws, int64_t ws_bytes,
+                float v_scale = 1.f) {
   CUtensorMap tq, tk, tv;
   int rc;
   const int qk_bytes = kQK8 ? 1 : 2;
   if ((rc = encode_map(&tq, q, BH, Lq, 128, 128, qk_bytes)) != DIT_ATTN_OK) return rc;
   if ((rc = encode_map(&tk, k, BH, Lk, 128, 64, qk_bytes)) != DIT_ATTN_OK) return rc;
-  if ((rc = encode_map(&tv, v, BH, Lk, 128, 128)) != DIT_ATTN_OK) return rc;
+  // a CTA's value half is 64 columns: 128 bytes of bf16 or 64 bytes of e4m3
+  if ((rc = kPV8 ? encode_map(&tv, v, BH, Lk, 128, 128, 1, 64) : encode_map(&tv, v, BH, Lk, 128, 128))
+      != DIT_ATTN_OK)
+    return rc;
   dit::Params p;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.Lq = Lq;
@@ -826,6 +839,8 @@ int launch_pair(const void* q, const void* k, const void* v, void* out, int64_t 
   p.num_qblocks = (Lq + kPairUnitRows - 1) / kPairUnitRows;
   p.num_units = static_cast<int>(BH * p.num_qblocks);
   p.scale_log2 = static_cast<float>(scale * 1.4426950408889634);
+  p.v_scale = v_scale;
+  p.inv_v_scale = 1.f / v_scale;
   SplitPlan plan = plan_split(p.num_units, (Lk + dit::kBN - 1) / dit::kBN, max_pairs);
   if (plan.splits > 1 && (!ws || ws_bytes < plan.ws_bytes))
     plan = SplitPlan{p.num_units, 1, p.num_units, 0, 0};
@@ -837,8 +852,8 @@ int launch_pair(const void* q, const void* k, const void* v, void* out, int64_t 
   const int pairs = p.num_items < max_pairs ? p.num_items : max_pairs;
   cudaLaunchAttribute attr;
   cudaLaunchConfig_t cfg =
-      pair_launch_config(2 * pairs, stream, &attr, dit::PairTraitsT<kQK8>::kSmemBytes);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, dit::fmha_fwd_pair_kernel<kQK8>, tq, tk, tv, p);
+      pair_launch_config(2 * pairs, stream, &attr, dit::PairTraitsT<kQK8, kPV8>::kSmemBytes);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, dit::fmha_fwd_pair_kernel<kQK8, kPV8>, tq, tk, tv, p);
   if (e != cudaSuccess) return cuda_fail(e);
   if (plan.splits > 1) {
     const int64_t rows = (plan.num_items - plan.split_base) / plan.splits * int64_t{kPairUnitRows};
@@ -853,29 +868,29 @@ int launch_pair(const void* q, const void* k, const void* v, void* out, int64_t 
 
 // Shared memory and cluster attributes of a pair kernel; *pairs = clusters of
 // two that fit on the device at once.
-template <bool kQK8>
+template <bool kQK8, bool kPV8>
 int setup_pair_kernel(int num_sms, int* pairs) {
-  const uint32_t smem = dit::PairTraitsT<kQK8>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(dit::fmha_fwd_pair_kernel<kQK8>,
+  const uint32_t smem = dit::PairTraitsT<kQK8, kPV8>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(dit::fmha_fwd_pair_kernel<kQK8, kPV8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e);
-  e = cudaFuncSetAttribute(dit::fmha_fwd_pair_kernel<kQK8>,
+  e = cudaFuncSetAttribute(dit::fmha_fwd_pair_kernel<kQK8, kPV8>,
                            cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
   if (e != cudaSuccess) return cuda_fail(e);
   cudaLaunchAttribute attr;
   cudaLaunchConfig_t cfg = pair_launch_config(num_sms, nullptr, &attr, smem);
   int clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&clusters, dit::fmha_fwd_pair_kernel<kQK8>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&clusters, dit::fmha_fwd_pair_kernel<kQK8, kPV8>, &cfg);
   if (e != cudaSuccess) return cuda_fail(e);
   if (clusters < 1) return cuda_fail(cudaErrorInvalidConfiguration);
   *pairs = clusters;
   return DIT_ATTN_OK;
 }
 
-// Argument checks shared by the bf16 and e4m3 forwards (qk_bytes = bytes per
-// element of q and k).
+// Argument checks shared by the bf16 and e4m3 forwards (qk_bytes, v_bytes =
+// bytes per element of q and k, of v).
 int check_forward_args(const void* q, const void* k, const void* v, const void* out, int B, int H,
-                       int Lq, int Lk, int d, float scale, int qk_bytes) {
+                       int Lq, int Lk, int d, float scale, int qk_bytes, int v_bytes = 2) {
   if (!q || !k || !v || !out) return DIT_ATTN_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || Lq < 1 || Lk < 1) return DIT_ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || scale < 0.f) return DIT_ATTN_ERR_INVALID_ARG;
@@ -888,10 +903,10 @@ int check_forward_args(const void* q, const void* k, const void* v, const void* 
   if (BH > INT_MAX || Lq > INT_MAX - 2 * dit::kUnitRows || Lk > INT_MAX - 2 * dit::kUnitRows ||
       BH * qblocks > INT_MAX)
     return DIT_ATTN_ERR_UNSUPPORTED;
-  const int64_t o_bytes = BH * Lq * d * 2, v_bytes = BH * Lk * d * 2;
+  const int64_t o_bytes = BH * Lq * d * 2, v_all = BH * Lk * d * v_bytes;
   const int64_t q_bytes = BH * Lq * d * qk_bytes, k_bytes = BH * Lk * d * qk_bytes;
   if (overlaps(out, o_bytes, q, q_bytes) || overlaps(out, o_bytes, k, k_bytes) ||
-      overlaps(out, o_bytes, v, v_bytes))
+      overlaps(out, o_bytes, v, v_all))
     return DIT_ATTN_ERR_INVALID_ARG;
   return DIT_ATTN_OK;
 }
@@ -900,15 +915,15 @@ int check_forward_args(const void* q, const void* k, const void* v, const void* 
 // no overlap with the tensors (NULL with size 0 runs unsplit).
 int check_workspace(const void* ws, long long ws_bytes, const void* q, const void* k,
                     const void* v, const void* out, int B, int H, int Lq, int Lk, int d,
-                    int qk_bytes) {
+                    int qk_bytes, int v_bytes = 2) {
   if (ws_bytes < 0 || (ws_bytes > 0 && !ws)) return DIT_ATTN_ERR_INVALID_ARG;
   if (!ws || ws_bytes == 0) return DIT_ATTN_OK;
   if (reinterpret_cast<uintptr_t>(ws) & 15u) return DIT_ATTN_ERR_INVALID_ARG;
   const int64_t BH = static_cast<int64_t>(B) * H;
-  const int64_t o_bytes = BH * Lq * d * 2, v_bytes = BH * Lk * d * 2;
+  const int64_t o_bytes = BH * Lq * d * 2, v_all = BH * Lk * d * v_bytes;
   const int64_t q_bytes = BH * Lq * d * qk_bytes, k_bytes = BH * Lk * d * qk_bytes;
   if (overlaps(ws, ws_bytes, q, q_bytes) || overlaps(ws, ws_bytes, k, k_bytes) ||
-      overlaps(ws, ws_bytes, v, v_bytes) || overlaps(ws, ws_bytes, out, o_bytes))
+      overlaps(ws, ws_bytes, v, v_all) || overlaps(ws, ws_bytes, out, o_bytes))
     return DIT_ATTN_ERR_INVALID_ARG;
   return DIT_ATTN_OK;
 }
@@ -958,13 +973,16 @@ int dit_attn_create(void) {
                            Traits<128>::kSmemBytes);
   if (e != cudaSuccess) return cuda_fail(e);
   {
-    int rc = DIT_ATTN_OK, bf16_pairs = 0, qk8_pairs = 0;
-    if ((rc = setup_pair_kernel<false>(prop.multiProcessorCount, &bf16_pairs)) != DIT_ATTN_OK)
+    int rc = DIT_ATTN_OK, bf16_pairs = 0, qk8_pairs = 0, fp8_pairs = 0;
+    if ((rc = setup_pair_kernel<false, false>(prop.multiProcessorCount, &bf16_pairs)) != DIT_ATTN_OK)
       return rc;
-    if ((rc = setup_pair_kernel<true>(prop.multiProcessorCount, &qk8_pairs)) != DIT_ATTN_OK)
+    if ((rc = setup_pair_kernel<true, false>(prop.multiProcessorCount, &qk8_pairs)) != DIT_ATTN_OK)
+      return rc;
+    if ((rc = setup_pair_kernel<true, true>(prop.multiProcessorCount, &fp8_pairs)) != DIT_ATTN_OK)
       return rc;
     g_state[dev].max_pairs = bf16_pairs;
     g_state[dev].max_pairs_qk8 = qk8_pairs;
+    g_state[dev].max_pairs_fp8 = fp8_pairs;
   }
   g_state[dev].num_sms = prop.multiProcessorCount;
   g_state[dev].ready = true;
@@ -998,8 +1016,8 @@ int dit_attn_forward_ws(const void* q, const void* k, const void* v, void* out, 
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return d == 64 ? launch<64>(q, k, v, out, BH, Lq, Lk, scale, s, num_sms)
-                 : launch_pair<false>(q, k, v, out, BH, Lq, Lk, scale, s, max_pairs, workspace,
-                                      workspace_bytes);
+                 : launch_pair<false, false>(q, k, v, out, BH, Lq, Lk, scale, s, max_pairs,
+                                             workspace, workspace_bytes);
 }
 
 int dit_attn_forward(const void* q, const void* k, const void* v, void* out, int B, int H, int Lq,
@@ -1029,9 +1047,9 @@ int dit_attn_forward_qk8_ws(const void* q8, const void* k8, const void* v, void*
     if (!g_state[dev].ready) return DIT_ATTN_ERR_NOT_INITIALIZED;
     max_pairs = g_state[dev].max_pairs_qk8;
   }
-  return launch_pair<true>(q8, k8, v, out, BH, Lq, Lk, logit_scale,
-                           static_cast<cudaStream_t>(stream), max_pairs, workspace,
-                           workspace_bytes);
+  return launch_pair<true, false>(q8, k8, v, out, BH, Lq, Lk, logit_scale,
+                                  static_cast<cudaStream_t>(stream), max_pairs, workspace,
+                                  workspace_bytes);
 }
 
 int dit_attn_forward_qk8(const void* q8, const void* k8, const void* v, void* out, int B, int H,
@@ -1039,6 +1057,43 @@ int dit_attn_forward_qk8(const void* q8, const void* k8, const void* v, void* ou
                          void* stream) {
   return dit_attn_forward_qk8_ws(q8, k8, v, out, B, H, Lq, Lk, d, scale, q_scale, k_scale,
                                  nullptr, 0, stream);
+}
+
+int dit_attn_forward_fp8_ws(const void* q8, const void* k8, const void* v8, void* out, int B,
+                            int H, int Lq, int Lk, int d, float scale, float q_scale,
+                            float k_scale, float v_scale, void* workspace,
+                            long long workspace_bytes, void* stream) {
+  int rc = check_forward_args(q8, k8, v8, out, B, H, Lq, Lk, d, scale, 1, 1);
+  if (rc != DIT_ATTN_OK) return rc;
+  if (!std::isfinite(q_scale) || !std::isfinite(k_scale) || q_scale < 0.f || k_scale < 0.f)
+    return DIT_ATTN_ERR_INVALID_ARG;
+  // 1/v_scale must be finite too: it scales the partial row sums of a split tail
+  if (!std::isfinite(v_scale) || !(v_scale > 0.f) || !std::isfinite(1.f / v_scale))
+    return DIT_ATTN_ERR_INVALID_ARG;
+  const double logit_scale = static_cast<double>(scale) * q_scale * k_scale;
+  if (!(logit_scale <= 3.0e38)) return DIT_ATTN_ERR_INVALID_ARG;
+  if (d != 128) return DIT_ATTN_ERR_UNSUPPORTED;
+  rc = check_workspace(workspace, workspace_bytes, q8, k8, v8, out, B, H, Lq, Lk, d, 1, 1);
+  if (rc != DIT_ATTN_OK) return rc;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  int dev = -1;
+  if (!current_device(&dev)) return DIT_ATTN_ERR_NO_DEVICE;
+  int max_pairs;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_state[dev].ready) return DIT_ATTN_ERR_NOT_INITIALIZED;
+    max_pairs = g_state[dev].max_pairs_fp8;
+  }
+  return launch_pair<true, true>(q8, k8, v8, out, BH, Lq, Lk, logit_scale,
+                                 static_cast<cudaStream_t>(stream), max_pairs, workspace,
+                                 workspace_bytes, v_scale);
+}
+
+int dit_attn_forward_fp8(const void* q8, const void* k8, const void* v8, void* out, int B, int H,
+                         int Lq, int Lk, int d, float scale, float q_scale, float k_scale,
+                         float v_scale, void* stream) {
+  return dit_attn_forward_fp8_ws(q8, k8, v8, out, B, H, Lq, Lk, d, scale, q_scale, k_scale,
+                                 v_scale, nullptr, 0, stream);
 }
 
 }  // extern "C"
@@ -1070,12 +1125,13 @@ int dit_attn_forward_noalloc(const void* q, const void* k, const void* v, void* 
   return dit_attn_forward_ws(q, k, v, out, B, H, Lq, Lk, d, scale, scratch, kScratchBytes, stream);
 }
 
-int dit_attn_workspace_size(int B, int H, int Lq, int Lk, int d, int qk8, long long* bytes) {
+int dit_attn_workspace_size(int B, int H, int Lq, int Lk, int d, int variant, long long* bytes) {
   if (!bytes) return DIT_ATTN_ERR_INVALID_ARG;
   *bytes = 0;
   if (B < 1 || H < 1 || Lq < 1 || Lk < 1) return DIT_ATTN_ERR_INVALID_ARG;
+  if (variant < 0 || variant > 2) return DIT_ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return DIT_ATTN_ERR_UNSUPPORTED;
-  if (qk8 && d != 128) return DIT_ATTN_ERR_UNSUPPORTED;
+  if (variant != 0 && d != 128) return DIT_ATTN_ERR_UNSUPPORTED;
   const int64_t BH = static_cast<int64_t>(B) * H;
   const int64_t qblocks = (static_cast<int64_t>(Lq) + dit::kUnitRows - 1) / dit::kUnitRows;
   if (BH > INT_MAX || Lq > INT_MAX - 2 * dit::kUnitRows || Lk > INT_MAX - 2 * dit::kUnitRows ||
@@ -1087,7 +1143,9 @@ int dit_attn_workspace_size(int B, int H, int Lq, int Lk, int d, int qk8, long l
   {
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_state[dev].ready) return DIT_ATTN_ERR_NOT_INITIALIZED;
-    max_pairs = qk8 ? g_state[dev].max_pairs_qk8 : g_state[dev].max_pairs;
+    max_pairs = variant == 2   ? g_state[dev].max_pairs_fp8
+                : variant == 1 ? g_state[dev].max_pairs_qk8
+                               : g_state[dev].max_pairs;
   }
   if (d == 64) return DIT_ATTN_OK;   // the d = 64 kernel never splits
   const int64_t units = BH * ((static_cast<int64_t>(Lq) + kPairUnitRows - 1) / kPairUnitRows);
@@ -1168,6 +1226,36 @@ int dit_attn_rmsnorm(const void* x, void* y, const void* weight, long long rows,
 int dit_attn_rmsnorm_e4m3(const void* x, void* y8, const void* weight, long long rows, int d,
                           float eps, float out_scale, void* stream) {
   return rmsnorm_impl(x, y8, weight, rows, d, eps, out_scale, 1, stream);
+}
+
+int dit_attn_quantize_e4m3(const void* x, void* y8, long long n, float out_scale, void* stream) {
+  if (!x || !y8 || n < 1) return DIT_ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(out_scale) || !(out_scale > 0.f)) return DIT_ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y8)) & 15u)
+    return DIT_ATTN_ERR_INVALID_ARG;
+  if (n > (static_cast<long long>(1) << 46)) return DIT_ATTN_ERR_UNSUPPORTED;
+  if (overlaps(x, static_cast<int64_t>(n) * 2, y8, n)) return DIT_ATTN_ERR_INVALID_ARG;
+  int dev = -1;
+  if (!current_device(&dev)) return DIT_ATTN_ERR_NO_DEVICE;
+  int num_sms;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_state[dev].ready) return DIT_ATTN_ERR_NOT_INITIALIZED;
+    num_sms = g_state[dev].num_sms;
+  }
+  const int64_t groups = n / 8;
+  const int tail = static_cast<int>(n % 8);
+  const int64_t per_block = 256 * dit::kQuantInFlight;
+  const int64_t want = (groups + per_block - 1) / per_block;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  const int grid = static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));
+  dit::quantize_e4m3_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(x), static_cast<uint2*>(y8), groups,
+      static_cast<const uint16_t*>(x) + groups * 8, static_cast<uint8_t*>(y8) + groups * 8, tail,
+      out_scale);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return DIT_ATTN_OK;
 }
 
 int dit_attn_get_device_error(void* stream) {

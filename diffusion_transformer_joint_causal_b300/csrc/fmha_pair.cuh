@@ -23,6 +23,16 @@
 // scale.  P and V stay bf16, so the second product and the softmax are
 // unchanged.  A query tile and a key half are one 128-byte-wide box each; the
 // shared memory this frees over bf16 holds two more pipeline stages.
+//
+// kPV8 (with kQK8) also takes e4m3 values: P is rounded to e4m3 in the softmax
+// (four keys per TMEM column, so P takes 16 of a half-row's 64 S columns) and
+// O += P V runs as kind::f8f6f4 with V's 128 keys x 64 columns per CTA in a
+// 64-byte-swizzled half.  Probabilities carry an offset of 2^3 against the
+// running max and the lazy rescale threshold is 5, so every stored p is at
+// most 448 (e4m3's largest finite value; 2^8 after a max pass) and at least
+// 2^-6 (its smallest normal) unless it is under 2^-9 of the row's largest;
+// the row sum adds the rounded values.  The per-tensor value scale is applied
+// with 1/l in the epilogue.
 #pragma once
 
 namespace dit {
@@ -41,8 +51,20 @@ constexpr int kPairLoadWarp = 17;
 constexpr int kPairRegsSoftmax = 112;
 constexpr int kPairRegsOther = 32;
 
-template <bool kQK8>
+// e4m3 probabilities: p = 2^(x - m + kProbOffsetE4M3) with the lazy rescale at
+// kRescaleThresholdE4M3, so p <= 2^8 after a max pass; an optimistic pass is
+// kept while its rounded row sum stays below 448 (no value saturated).  With
+// RMS-normalised logits the row sum of a key tile is about 2^7 at this
+// offset, so the optimistic pass holds; at 2^4 it would exceed 448 on most
+// warp steps.
+constexpr float kProbOffsetE4M3 = 3.0f;
+constexpr float kRescaleThresholdE4M3 = 5.0f;
+constexpr float kOptimisticSumLimitE4M3 = 448.0f;
+
+template <bool kQK8, bool kPV8 = false>
 struct PairTraitsT {
+  static_assert(kQK8 || !kPV8, "e4m3 values come with e4m3 queries and keys");
+  static constexpr bool kP8 = kPV8;
   static constexpr int D = 128;
   static constexpr int kBoxCols = 64;                       // bf16 columns in a 128-byte box row
   static constexpr int kQKBoxes = kQK8 ? 1 : 2;             // 128-byte boxes across d for Q, K
@@ -50,8 +72,9 @@ struct PairTraitsT {
   static constexpr uint32_t kQTileBytes = kQKBoxes * kQBoxBytes;   // one 128-row query tile
   static constexpr uint32_t kKBoxBytes = 64u * 128u;        // 64 keys x 128 bytes
   static constexpr uint32_t kKHalfBytes = kQKBoxes * kKBoxBytes;   // one K half
-  static constexpr uint32_t kHalfBytes = 16384;             // a stage: one V half (or K half)
-  static constexpr int kStages = kQK8 ? 10 : 8;
+  static constexpr uint32_t kVHalfBytes = kPV8 ? 128u * 64u : 128u * 128u;  // 128 keys x 64 columns
+  static constexpr uint32_t kHalfBytes = kPV8 ? 8192 : 16384;  // a stage: one V half (or K half)
+  static constexpr int kStages = kPV8 ? 20 : (kQK8 ? 10 : 8);
   __host__ __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
   __host__ __device__ static constexpr uint32_t col_o(int t) { return 256u + 128u * t; }
   static constexpr uint32_t kTmemCols = 512;
@@ -74,10 +97,10 @@ struct PairTraitsT {
 using PairTraits = PairTraitsT<false>;
 
 // ----------------------------------------------------------------- producer (both CTAs)
-template <bool kQK8>
+template <bool kQK8, bool kPV8>
 __device__ void pair_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                const CUtensorMap* tmV, const Params& p, const Shared& sh) {
-  using T = PairTraitsT<kQK8>;
+  using T = PairTraitsT<kQK8, kPV8>;
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
   const uint64_t pol_kv = policy_evict_last();
@@ -131,10 +154,10 @@ __device__ void pair_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
         if (!ok) break;
       }
       // V half: keys j*128 .. +127, columns 64*rank .. +63
-      ok = take_empty(T::kHalfBytes);
+      ok = take_empty(T::kVHalfBytes);
       if (!ok) break;
       tma_load_3d_pair(sh.base + T::kOffKV + stage * T::kHalfBytes, tmV, full0_leader + 8u * stage,
-                       static_cast<int>(rank) * T::kBoxCols, j * kBN, bh, pol_kv);
+                       static_cast<int>(rank) * 64, j * kBN, bh, pol_kv);
       advance();
     }
   }
@@ -165,7 +188,7 @@ __device__ void pair_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
 // ----------------------------------------------------------------- MMA issuer (leader CTA)
 template <bool kQK8>
 __device__ __forceinline__ void pair_issue_qk(uint32_t d_tmem, uint32_t q_lo, uint32_t k_lo) {
-  using T = PairTraitsT<kQK8>;
+  using T = PairTraitsT<kQK8, false>;
   constexpr uint32_t hi = desc_hi_sw128(1024);
   if constexpr (kQK8) {
     // one 128-byte box row holds all of d; each instruction takes 32 bytes of it
@@ -185,19 +208,31 @@ __device__ __forceinline__ void pair_issue_qk(uint32_t d_tmem, uint32_t q_lo, ui
   }
 }
 
+template <bool kPV8>
 __device__ __forceinline__ void pair_issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_lo,
                                               bool accumulate) {
-  constexpr uint32_t idesc = idesc_bf16_f32(2 * kBM, PairTraits::D, 0, 1);
-  constexpr uint32_t hi = desc_hi_sw128(1024);
+  if constexpr (kPV8) {
+    // e4m3 P of keys [64h, 64h+64) is in S columns [64h, 64h+16); V rows are
+    // 64 bytes, so 32 keys (one instruction) span 2048 bytes
+    constexpr uint32_t idesc = idesc_e4m3_f32(2 * kBM, PairTraits::D, 0, 1);
+    constexpr uint32_t hi = desc_hi_sw64(512);
 #pragma unroll
-  for (int k = 0; k < kBN / 16; ++k)   // P of keys [64h, 64h+64) is in S columns [64h, 64h+32)
-    mma_ts_lo_pair(d_tmem, p_tmem + (k / 4) * 64 + (k % 4) * 8, v_lo + ((k * 16 * 128) >> 4), hi,
-                   idesc, (accumulate || k > 0) ? 1u : 0u);
+    for (int k = 0; k < kBN / 32; ++k)
+      mma_ts_lo_pair_f8(d_tmem, p_tmem + (k / 2) * 64 + (k % 2) * 8,
+                        v_lo + ((k * 32 * 64) >> 4), hi, idesc, (accumulate || k > 0) ? 1u : 0u);
+  } else {
+    constexpr uint32_t idesc = idesc_bf16_f32(2 * kBM, PairTraits::D, 0, 1);
+    constexpr uint32_t hi = desc_hi_sw128(1024);
+#pragma unroll
+    for (int k = 0; k < kBN / 16; ++k)   // P of keys [64h, 64h+64) is in S columns [64h, 64h+32)
+      mma_ts_lo_pair(d_tmem, p_tmem + (k / 4) * 64 + (k % 4) * 8, v_lo + ((k * 16 * 128) >> 4),
+                     hi, idesc, (accumulate || k > 0) ? 1u : 0u);
+  }
 }
 
-template <bool kQK8>
+template <bool kQK8, bool kPV8>
 __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) {
-  using T = PairTraitsT<kQK8>;
+  using T = PairTraitsT<kQK8, kPV8>;
   constexpr uint16_t kBoth = 3;
   const bool issuer = (threadIdx.x & 31) == 0;
   uint32_t stage = 0, phase = 0, g = 0, it = 0;
@@ -257,7 +292,7 @@ __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) 
       if (!ok) break;
       tc_fence_after();
       if (issuer) {
-        pair_issue_pv(tmem + T::col_o(0), tmem + T::col_s(0), kv_lo(sV), j > 0);
+        pair_issue_pv<kPV8>(tmem + T::col_o(0), tmem + T::col_s(0), kv_lo(sV), j > 0);
         if (more) {
           pair_issue_qk<kQK8>(tmem + T::col_s(0), q_lo0, kv_lo(sK_next));
           mma_commit_pair(sh.bar(T::kBarSFull + 0), kBoth);
@@ -272,7 +307,7 @@ __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) 
       if (!ok) break;
       tc_fence_after();
       if (issuer) {
-        pair_issue_pv(tmem + T::col_o(1), tmem + T::col_s(1), kv_lo(sV), j > 0);
+        pair_issue_pv<kPV8>(tmem + T::col_o(1), tmem + T::col_s(1), kv_lo(sV), j > 0);
         if (more) {
           pair_issue_qk<kQK8>(tmem + T::col_s(1), q_lo1, kv_lo(sK_next));
           mma_commit_pair(sh.bar(T::kBarEmpty + sV), kBoth);
@@ -314,25 +349,60 @@ __device__ __forceinline__ float rowmax_chunk(const uint32_t (&sr)[32], int key0
   return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
 }
 
+// Probabilities of 32 logits rounded to e4m3, four keys per word (key order =
+// byte order), and the sum of the rounded values added into acc.
+template <bool kMasked>
+__device__ __forceinline__ void probs_chunk_e4m3(const uint32_t (&sr)[32], float scale_log2,
+                                                 float neg_m, int key0, int valid, uint32_t* pk,
+                                                 float (&acc)[8]) {
+  const float2 sl2 = make_float2(scale_log2, scale_log2);
+  const float2 nm = make_float2(neg_m, neg_m);
+#pragma unroll
+  for (int i = 0; i < 32; i += 4) {
+    const float2 x01 =
+        __ffma2_rn(make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), sl2, nm);
+    const float2 x23 =
+        __ffma2_rn(make_float2(__uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3])), sl2, nm);
+    float p0 = ex2_approx(x01.x), p1 = ex2_approx(x01.y);
+    float p2 = ex2_approx(x23.x), p3 = ex2_approx(x23.y);
+    if (kMasked) {
+      p0 = (key0 + i < valid) ? p0 : 0.f;
+      p1 = (key0 + i + 1 < valid) ? p1 : 0.f;
+      p2 = (key0 + i + 2 < valid) ? p2 : 0.f;
+      p3 = (key0 + i + 3 < valid) ? p3 : 0.f;
+    }
+    pk[i / 4] = pack_e4m3x4_sum(p0, p1, p2, p3, acc[(i / 4) & 3], acc[4 + ((i / 4) & 3)]);
+  }
+}
+
 // One query tile's softmax step for this thread's half-row (keys key0 ..
 // key0+63 of the tile) with a small register footprint: the logits are read
 // from TMEM 32 columns at a time, and the probabilities of both chunks are
-// stored once, at the end, over the half-row's first 32 S columns, so that a
-// recompute can read the logits again.  Otherwise as softmax_tile_half.
-template <int D, class ORescale>
+// stored once, at the end, over the half-row's first S columns (32 for bf16,
+// 16 for e4m3), so that a recompute can read the logits again.  Otherwise as
+// softmax_tile_half.
+template <int D, bool kP8, class ORescale>
 __device__ __forceinline__ void softmax_tile_lean(uint32_t taddr_s, int key0, bool first,
                                                   bool masked, int valid, float scale_log2,
                                                   float& m_used, float& l, ORescale&& o_rescale) {
+  constexpr int kPWords = kP8 ? 8 : 16;   // packed probability words per 32 keys
+  constexpr float kThreshold = kP8 ? kRescaleThresholdE4M3 : kRescaleThreshold;
   uint32_t sr[32];
-  uint32_t pk[32];
+  uint32_t pk[2 * kPWords];
   float acc[8];
   auto load = [&](int c) {
     tmem_ld16x2_32<64>(taddr_s + 32 * c, sr);
     tmem_wait_ld();
   };
   auto probs = [&](int c, float m) {
-    if (masked) probs_chunk<true>(sr, scale_log2, -m, key0 + 32 * c, valid, &pk[16 * c], acc);
-    else probs_chunk<false>(sr, scale_log2, -m, key0 + 32 * c, kBN, &pk[16 * c], acc);
+    if constexpr (kP8) {
+      const float neg_m = kProbOffsetE4M3 - m;
+      if (masked) probs_chunk_e4m3<true>(sr, scale_log2, neg_m, key0 + 32 * c, valid, &pk[8 * c], acc);
+      else probs_chunk_e4m3<false>(sr, scale_log2, neg_m, key0 + 32 * c, kBN, &pk[8 * c], acc);
+    } else {
+      if (masked) probs_chunk<true>(sr, scale_log2, -m, key0 + 32 * c, valid, &pk[16 * c], acc);
+      else probs_chunk<false>(sr, scale_log2, -m, key0 + 32 * c, kBN, &pk[16 * c], acc);
+    }
   };
   auto chunk_max = [&](int c) -> float {
     return masked ? rowmax_chunk<true>(sr, key0 + 32 * c, valid)
@@ -352,7 +422,7 @@ __device__ __forceinline__ void softmax_tile_lean(uint32_t taddr_s, int key0, bo
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
     const float m_tile = mx * scale_log2;
     float factor = 1.f;
-    if (m_tile > m_used + kRescaleThreshold) {
+    if (m_tile > m_used + kThreshold) {
       factor = ex2_approx(m_used - m_tile);   // 0 on the first tile
       l *= factor;
       m_used = m_tile;
@@ -369,17 +439,24 @@ __device__ __forceinline__ void softmax_tile_lean(uint32_t taddr_s, int key0, bo
   } else {
     // Optimistic pass against the running max; a rounded row sum above 2^16
     // means some p > 2^9: raise the max (always by more than 8), rescale l
-    // and O, recompute.  Warp-uniform branch.
+    // and O, recompute.  With e4m3 P a row sum of 448 or more may hide a
+    // saturated value: take the max pass.  Warp-uniform branch.
     load(0);
     probs(0, m_used);
     load(1);
     probs(1, m_used);
     const float half_sum = sum8(acc);
     const float row_sum = half_sum + __shfl_xor_sync(0xffffffffu, half_sum, 16);
-    if (__any_sync(0xffffffffu, !(row_sum <= kOptimisticSumLimit))) max_pass();
+    const bool redo = kP8 ? !(row_sum < kOptimisticSumLimitE4M3)
+                          : !(row_sum <= kOptimisticSumLimit);
+    if (__any_sync(0xffffffffu, redo)) max_pass();
   }
-  tmem_st16x2_16<64>(taddr_s, &pk[0]);
-  tmem_st16x2_16<64>(taddr_s + 16, &pk[16]);
+  if constexpr (kP8) {
+    tmem_st16x2_16<64>(taddr_s, &pk[0]);
+  } else {
+    tmem_st16x2_16<64>(taddr_s, &pk[0]);
+    tmem_st16x2_16<64>(taddr_s + 16, &pk[16]);
+  }
   l += sum8(acc);
 }
 
@@ -421,8 +498,8 @@ __device__ void softmax_role_pair(const Params& p, const Shared& sh, uint32_t tm
       tc_fence_after();
       // O_t is quiescent here: S_t's completion implies the previous P.V
       // product into O_t finished.
-      softmax_tile_lean<D>(taddr_s, key0, j == w.j0, masked, valid, scale_log2, m_used, l,
-                           [&](float f) { rescale_o_half<D>(taddr_o, f); });
+      softmax_tile_lean<D, T::kP8>(taddr_s, key0, j == w.j0, masked, valid, scale_log2, m_used,
+                                   l, [&](float f) { rescale_o_half<D>(taddr_o, f); });
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -436,12 +513,13 @@ __device__ void softmax_role_pair(const Params& p, const Shared& sh, uint32_t tm
     tc_fence_after();
     const float l_row = l + __shfl_xor_sync(0xffffffffu, l, 16);
     const int prow = rank * kUnitRows + t * kBM + r;   // row within the 512-row unit
+    // e4m3 values: out = v_scale * O / l; a partial row keeps O and l / v_scale
     if (w.chunk >= 0) {
       store_partial<D>(p, static_cast<int64_t>(w.chunk) * (2 * kUnitRows) + prow, half, taddr_o,
-                       m_used, l_row);
+                       m_used, T::kP8 ? l_row * p.inv_v_scale : l_row);
       continue;
     }
-    const float inv_l = 1.f / l_row;
+    const float inv_l = T::kP8 ? p.v_scale / l_row : 1.f / l_row;
     const int row = w.qblock * (2 * kUnitRows) + prow;
     const bool row_ok = row < p.Lq;
     uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<int64_t>(w.bh) * p.Lq + row) * D +
@@ -467,12 +545,12 @@ __device__ void softmax_role_pair(const Params& p, const Shared& sh, uint32_t tm
 
 // ----------------------------------------------------------------- kernel
 // Launched with a cluster dimension of 2 (consecutive CTAs form a pair).
-template <bool kQK8>
+template <bool kQK8, bool kPV8>
 __global__ void __launch_bounds__(kPairThreads, 1)
     fmha_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const Params p) {
-  using T = PairTraitsT<kQK8>;
+  using T = PairTraitsT<kQK8, kPV8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -523,10 +601,10 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     softmax_role_pair<T::D, T>(p, sh, tmem);
   } else if (warp == kPairMmaWarp) {
     reg_dealloc<kPairRegsOther>();
-    if (leader) pair_mma_role<kQK8>(p, sh, tmem);
+    if (leader) pair_mma_role<kQK8, kPV8>(p, sh, tmem);
   } else if (warp == kPairLoadWarp) {
     reg_dealloc<kPairRegsOther>();
-    if (lane == 0) pair_load_role<kQK8>(&tmQ, &tmK, &tmV, p, sh);
+    if (lane == 0) pair_load_role<kQK8, kPV8>(&tmQ, &tmK, &tmV, p, sh);
     __syncwarp();
   } else {
     reg_dealloc<kPairRegsOther>();

@@ -409,6 +409,18 @@ __device__ __forceinline__ void mma_ts_lo_pair(uint32_t d_tmem, uint32_t a_tmem,
       "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// The same with e4m3 A (TMEM) and B (shared memory): 32 bytes of K per instruction.
+__device__ __forceinline__ void mma_ts_lo_pair_f8(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                                  uint32_t hi, uint32_t idesc,
+                                                  uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrive on the mbarrier at the same offset in every CTA of `cta_mask` once
 // all prior pair MMAs of this thread have completed.
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask) {
@@ -455,6 +467,12 @@ __host__ __device__ constexpr uint32_t desc_hi_sw128(uint32_t sbo_bytes) {
   return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
 }
 
+// High word of the 64-byte-swizzle descriptor (layout type 4): rows of 64
+// bytes, 8-row atoms of 512 bytes.
+__host__ __device__ constexpr uint32_t desc_hi_sw64(uint32_t sbo_bytes) {
+  return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (4u << 29);
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B and an fp32 accumulator.
 // a_mn / b_mn select MN-major (transposed) operands; N at bits [17,23) as N>>3,
 // M at bits [24,29) as M>>4.
@@ -468,10 +486,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
          | (static_cast<uint32_t>(M >> 4) << 24);   // M
 }
 
-// Instruction descriptor for kind::f8f6f4 with e4m3 A/B (format code 0, both
-// K-major) and an fp32 accumulator.
-__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+// Instruction descriptor for kind::f8f6f4 with e4m3 A/B (format code 0) and
+// an fp32 accumulator; a_mn / b_mn select MN-major operands (default K-major).
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, int a_mn = 0, int b_mn = 0) {
   return (1u << 4)                                  // D format: f32
+         | (static_cast<uint32_t>(a_mn) << 15)      // A major
+         | (static_cast<uint32_t>(b_mn) << 16)      // B major
          | (static_cast<uint32_t>(N >> 3) << 17)    // N
          | (static_cast<uint32_t>(M >> 4) << 24);   // M
 }
@@ -498,6 +518,29 @@ __device__ __forceinline__ void add_bf16x2_halves(float& lo_acc, float& hi_acc, 
       "add.rn.f32.bf16 %1, hi, %1;\n\t}"
       : "+f"(lo_acc), "+f"(hi_acc)
       : "r"(w));
+}
+
+// Four non-negative fp32 -> four e4m3 bytes (round to nearest even,
+// saturating at 448), p0 in bits [7:0] .. p3 in bits [31:24]; the rounded
+// values are added to acc0 (p0 + p2) and acc1 (p1 + p3).  The e4m3 -> f16
+// widening is exact; the pairwise f16 sum is exact unless the two values'
+// exponents differ by more than 7 (then it rounds at 2^-11 relative).
+__device__ __forceinline__ uint32_t pack_e4m3x4_sum(float p0, float p1, float p2, float p3,
+                                                    float& acc0, float& acc1) {
+  uint32_t w;
+  asm("{\n\t.reg .b16 lo, hi, s0, s1;\n\t.reg .b32 flo, fhi, fs;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %4, %3;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %6, %5;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t"
+      "cvt.rn.f16x2.e4m3x2 flo, lo;\n\t"
+      "cvt.rn.f16x2.e4m3x2 fhi, hi;\n\t"
+      "add.rn.f16x2 fs, flo, fhi;\n\t"
+      "mov.b32 {s0, s1}, fs;\n\t"
+      "add.rn.f32.f16 %1, s0, %1;\n\t"
+      "add.rn.f32.f16 %2, s1, %2;\n\t}"
+      : "=r"(w), "+f"(acc0), "+f"(acc1)
+      : "f"(p0), "f"(p1), "f"(p2), "f"(p3));
+  return w;
 }
 
 // Two fp32 -> packed bf16x2 (round to nearest even); lo goes to bits [15:0].

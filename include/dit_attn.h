@@ -107,12 +107,13 @@ int dit_attn_forward_noalloc(const void* q, const void* k, const void* v, void* 
                              int Lq, int Lk, int d, float scale, void* stream);
 
 /*
- * Workspace bytes that dit_attn_forward_ws (qk8 = 0) or dit_attn_forward_qk8_ws
- * (qk8 = 1) uses for these sizes on the current device; 0 when no split
- * applies (d = 64, or the last wave is full or its units too short).  Size
+ * Workspace bytes that dit_attn_forward_ws (variant 0), dit_attn_forward_qk8_ws
+ * (variant 1) or dit_attn_forward_fp8_ws (variant 2) uses for these sizes on
+ * the current device; 0 when no split applies (d = 64, or the last wave is
+ * full or its units too short).  Another variant is INVALID_ARG.  Size
  * arguments as for the forward calls; requires dit_attn_create().
  */
-int dit_attn_workspace_size(int B, int H, int Lq, int Lk, int d, int qk8, long long* bytes);
+int dit_attn_workspace_size(int B, int H, int Lq, int Lk, int d, int variant, long long* bytes);
 
 /*
  * The same attention with e4m3 queries and keys ("cuDNN FP8 attention" is the
@@ -147,6 +148,54 @@ int dit_attn_forward_qk8_ws(const void* q8, const void* k8, const void* v, void*
                             int H, int Lq, int Lk, int d, float scale, float q_scale,
                             float k_scale, void* workspace, long long workspace_bytes,
                             void* stream);
+
+/*
+ * The same attention with e4m3 queries, keys and values, P rounded to e4m3
+ * before P.V (the FP8 attention the two pages above compare with BF16; the
+ * pages print no recipe, so this follows the plainest reading: per-tensor
+ * scales for Q, K and V):
+ *
+ *     s_ij = scale * q_scale * k_scale * sum_c e4m3(q8[b,h,i,c]) * e4m3(k8[b,h,j,c])
+ *     p_ij = e4m3( 2^(s_ij * log2(e) - m_i + 3) ),  m_i a running row max (log2 units)
+ *     o[b,h,i,:] = v_scale * sum_j p_ij * e4m3(v8[b,h,j,:]) / sum_j p_ij
+ *
+ * q8, k8 as in dit_attn_forward_qk8; v8: device pointer, e4m3 codes,
+ * contiguous [B, H, Lk, d], dequantised value = code value * v_scale.  out:
+ * bf16 [B, H, Lq, d].  d must be 128 (else UNSUPPORTED).  q_scale, k_scale
+ * finite and >= 0, v_scale finite and > 0 with a finite reciprocal, and
+ * scale*q_scale*k_scale at most 3e38 (else INVALID_ARG).  Arithmetic: both
+ * products on e4m3 tensor cores with exact fp32 accumulation; every p is
+ * rounded to e4m3 (relative error at most 2^-4 where p >= 2^-6, i.e. for
+ * every key within 2^-9 of the row's largest weight), and the row sum adds
+ * the rounded p, so the output is a convex combination of the dequantised
+ * value rows.  Sizes (q8, k8, v8 counted in bytes), alignment, overlap,
+ * stream and error behaviour as in dit_attn_forward; NaN codes as in
+ * dit_attn_forward_qk8.
+ */
+int dit_attn_forward_fp8(const void* q8, const void* k8, const void* v8, void* out, int B, int H,
+                         int Lq, int Lk, int d, float scale, float q_scale, float k_scale,
+                         float v_scale, void* stream);
+
+/* dit_attn_forward_fp8 with a workspace, as dit_attn_forward_ws. */
+int dit_attn_forward_fp8_ws(const void* q8, const void* k8, const void* v8, void* out, int B,
+                            int H, int Lq, int Lk, int d, float scale, float q_scale,
+                            float k_scale, float v_scale, void* workspace,
+                            long long workspace_bytes, void* stream);
+
+/*
+ * Per-tensor e4m3 quantisation (the prologue that gives dit_attn_forward_fp8
+ * its values, or e4m3 queries and keys that are not RMS-normalised):
+ *
+ *     y8[i] = e4m3( x[i] * out_scale ),  i < n
+ *
+ * the product in fp32; e4m3() as in dit_attn_rmsnorm_e4m3 (nearest even,
+ * saturating at +-448; NaN stays NaN).  out_scale is the reciprocal of the
+ * dequantisation scale handed to the forward (for example 448 / max|x|).
+ * x: device bf16 [n]; y8: device [n] bytes, not overlapping x; both 16-byte
+ * aligned; n >= 1; out_scale finite and > 0 (else INVALID_ARG).  Enqueued on
+ * `stream`; requires dit_attn_create().
+ */
+int dit_attn_quantize_e4m3(const void* x, void* y8, long long n, float out_scale, void* stream);
 
 /*
  * RMS normalisation of queries or keys over the head dimension, per token and

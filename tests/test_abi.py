@@ -228,3 +228,89 @@ def test_workspace_entry_points_no_device():
     assert dit.forward_ws_ptr(A, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 8, 8, 64, 0.125, 0, 0) == 4
     with pytest.raises(dit.DitAttnError):
         dit.workspace_size(1, 24, 16896, 16896, 128)
+
+
+# ----------------------------------------------------------------- e4m3 Q/K/V forward, quantise
+
+FP8 = (A, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 8, 8, 128, 0.125, 0.02, 0.03, 0.01)
+
+
+def _fp8(**change):
+    names = ("q8", "k8", "v8", "out", "B", "H", "Lq", "Lk", "d", "scale", "q_scale", "k_scale",
+             "v_scale")
+    args = dict(zip(names, FP8))
+    args.update(change)
+    return tuple(args[n] for n in names)
+
+
+@pytest.mark.parametrize("args,expect", [
+    (_fp8(v8=0), 1),                                  # null v8
+    (_fp8(Lq=0), 1),                                  # Lq = 0
+    (_fp8(v8=A + 2 * MB + 4), 1),                     # misaligned v8
+    (_fp8(v_scale=0.0), 1),                           # v_scale must be > 0
+    (_fp8(v_scale=-0.5), 1),
+    (_fp8(v_scale=float("nan")), 1),
+    (_fp8(v_scale=float("inf")), 1),
+    (_fp8(v_scale=1e-45), 1),                         # 1 / v_scale overflows fp32
+    (_fp8(q_scale=-1.0), 1),
+    (_fp8(scale=1e20, q_scale=1e20, k_scale=1e20), 1),
+    (_fp8(out=A + 2 * MB + 512), 1),                  # out overlaps the 1 KB of v8
+    (_fp8(d=64), 2),                                  # d = 128 only
+    (_fp8(B=65536, H=65536), 2),
+])
+def test_forward_fp8_rejects_bad_arguments(args, expect):
+    assert dit.forward_fp8_ptr(*args) == expect
+
+
+@pytest.mark.parametrize("ws,nbytes,expect", [
+    (WS, -1, 1), (0, 4096, 1), (WS + 8, 4096, 1),
+    (A + 2 * MB, 4096, 1),       # overlaps v8
+])
+def test_forward_fp8_ws_rejects_bad_workspace(ws, nbytes, expect):
+    assert dit.forward_fp8_ws_ptr(*FP8, ws, nbytes) == expect
+
+
+@pytest.mark.skipif(_has_gpu(), reason="a valid call with fake pointers must not reach a GPU")
+def test_fp8_entry_points_no_device():
+    # v8 is 1 KB of e4m3 codes: an out right after it does not overlap
+    assert dit.forward_fp8_ptr(*_fp8(out=A + 2 * MB + 1024)) == 4
+    assert dit.forward_fp8_ws_ptr(*FP8, WS, 4096) == 4
+    assert dit.quantize_e4m3_ptr(A, A + 2048, 1000, 2.0) == 4     # y8 right after x
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((0, A + MB, 100, 1.0), 1),                       # null x
+    ((A, 0, 100, 1.0), 1),                            # null y8
+    ((A, A + MB, 0, 1.0), 1),                         # n = 0
+    ((A, A + MB, -5, 1.0), 1),
+    ((A, A + MB, 100, 0.0), 1),                       # out_scale must be > 0
+    ((A, A + MB, 100, float("nan")), 1),
+    ((A, A + MB, 100, float("inf")), 1),
+    ((A + 2, A + MB, 100, 1.0), 1),                   # misaligned x
+    ((A, A + MB + 8, 100, 1.0), 1),                   # misaligned y8
+    ((A, A + 192, 100, 1.0), 1),                      # y8 overlaps x (200 bytes of bf16)
+    ((A, A + MB, 1 << 50, 1.0), 2),                   # too large
+])
+def test_quantize_e4m3_rejects_bad_arguments(args, expect):
+    assert dit.quantize_e4m3_ptr(*args) == expect
+
+
+def test_workspace_size_variants_validate_before_cuda():
+    lib = ctypes.CDLL(dit.library_path())
+    lib.dit_attn_workspace_size.argtypes = [ctypes.c_int] * 6 + [ctypes.c_void_p]
+    nb = ctypes.c_longlong(7)
+    assert lib.dit_attn_workspace_size(1, 1, 8, 8, 128, 3, ctypes.byref(nb)) == 1 and nb.value == 0
+    assert lib.dit_attn_workspace_size(1, 1, 8, 8, 128, -1, ctypes.byref(nb)) == 1
+    assert lib.dit_attn_workspace_size(1, 1, 8, 8, 64, 2, ctypes.byref(nb)) == 2   # d = 128 only
+
+
+def test_python_fp8_wrappers_check_tensors():
+    import torch
+    x = torch.zeros(1, 1, 8, 128, dtype=torch.bfloat16)
+    x8 = torch.zeros(1, 1, 8, 128, dtype=torch.uint8)
+    with pytest.raises(TypeError):
+        dit.forward_fp8(x8, x8, x, 1.0, 1.0, 1.0)          # bf16 v / CPU tensors
+    with pytest.raises(TypeError):
+        dit.forward_fp8(x8, x8, x8, 1.0, 1.0, 1.0)         # CPU tensors
+    with pytest.raises(TypeError):
+        dit.quantize_e4m3(x, 1.0)                          # CPU tensor
