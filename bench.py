@@ -62,9 +62,11 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the per-workload timing sweep (eager and CUDA-graph replay)")
-    ap.add_argument("--path", choices=["bf16", "qk8"], default="bf16",
+    ap.add_argument("--path", choices=["bf16", "qk8", "fp8"], default="bf16",
                     help="bf16: dit.forward; qk8: e4m3 Q/K (RMS-norm + quantising prologue, "
-                         "outside the device-timed region) and dit.forward_qk8")
+                         "outside the device-timed region) and dit.forward_qk8; fp8: e4m3 "
+                         "Q/K as qk8 plus e4m3 V (dit.quantize_e4m3 at a calibrated "
+                         "per-tensor scale) and dit.forward_fp8")
     return ap.parse_args()
 
 
@@ -404,17 +406,23 @@ def rmsnorm_roofline(dit, dev, peaks, calls: int = 20):
                          "frac": gbs / peaks["hbm"], "peak_source": f"{peaks['source']} copy"}}
 
 
-def qk8_sweep(dit, dev, peaks, bf16_ms: dict, calls: int = 20):
-    """The e4m3-QK path on the RMS-normalised workloads: the quantising
-    prologue (dit.rmsnorm_e4m3 of Q and of K, out_scale 448/sqrt(d)) and the
-    e4m3-QK forward, each timed with CUDA events over `calls` launches.  S = Q
-    K^T runs at the e4m3 tensor rate (nominally 2x bf16) and P V at the bf16
-    rate, so the contraction's mixed peak is 4/3 of the bf16 one."""
+def e4m3_sweep(dit, dev, peaks, bf16_ms: dict, calls: int = 20):
+    """The e4m3 paths on the RMS-normalised workloads, each timed with CUDA
+    events over `calls` launches of its prologue and of its forward.
+
+    qk8: the quantising prologue (dit.rmsnorm_e4m3 of Q and of K, out_scale
+    448/sqrt(d)) and the e4m3-QK forward.  S = Q K^T runs at the e4m3 tensor
+    rate (nominally 2x bf16) and P V at the bf16 rate, so the contraction's
+    mixed peak is 4/3 of the bf16 one.
+    fp8: the same prologue plus dit.quantize_e4m3 of V (at the calibrated
+    scale max|V|/448) and the e4m3 Q/K/V forward; both products run at the
+    e4m3 rate (peak 2x bf16).
+    Returns ({workload: qk8 result}, {workload: fp8 result})."""
     import numpy as np
     import torch
 
     import workloads as W
-    res = {}
+    res = {"qk8": {}, "fp8": {}}
     for w in W.WORKLOADS:
         if not w.rms_norm or w.d != 128:
             continue
@@ -424,45 +432,61 @@ def qk8_sweep(dit, dev, peaks, bf16_ms: dict, calls: int = 20):
         s = float(np.float32(math.sqrt(w.d) / 448.0))
         q8 = torch.empty(q.shape, dtype=torch.float8_e4m3fn, device=dev)
         k8 = torch.empty(k.shape, dtype=torch.float8_e4m3fn, device=dev)
+        v8 = torch.empty(v.shape, dtype=torch.float8_e4m3fn, device=dev)
+        vs = v_calibration(v)
         out = torch.empty_like(q)
+        for mode in ("qk8", "fp8"):
+            fp8 = mode == "fp8"
 
-        def prologue():
-            dit.rmsnorm_e4m3(q, inv, out=q8)
-            dit.rmsnorm_e4m3(k, inv, out=k8)
+            def prologue():
+                dit.rmsnorm_e4m3(q, inv, out=q8)
+                dit.rmsnorm_e4m3(k, inv, out=k8)
+                if fp8:
+                    dit.quantize_e4m3(v, 1.0 / vs, out=v8)
 
-        def attn():
-            dit.forward_qk8(q8, k8, v, s, s, w.scale, out=out)
+            def attn():
+                if fp8:
+                    dit.forward_fp8(q8, k8, v8, s, s, vs, w.scale, out=out)
+                else:
+                    dit.forward_qk8(q8, k8, v, s, s, w.scale, out=out)
 
-        for _ in range(3):
-            prologue()
-            attn()
-        torch.cuda.synchronize(dev)
-        times = {}
-        for name, fn in (("prologue", prologue), ("attention", attn)):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            for _ in range(calls):
-                fn()
-            e1.record()
+            for _ in range(3):
+                prologue()
+                attn()
             torch.cuda.synchronize(dev)
-            times[name] = e0.elapsed_time(e1) / calls
-        tf = w.flops / times["attention"] / 1e9
-        mixed_peak = peaks["bf16"] * 4.0 / 3.0
-        nbytes = (q.numel() + k.numel()) * 3.0
-        res[w.name] = {
-            "shape": [w.B, w.H, w.Lq, w.Lk, w.d],
-            "ms_attention": times["attention"], "tflops": tf,
-            "speedup_vs_bf16_eager": bf16_ms[w.name] / times["attention"]
-            if w.name in bf16_ms else None,
-            "frac_of_bf16_peak": tf / peaks["bf16"],
-            "frac_of_mixed_peak": tf / mixed_peak,
-            "ms_prologue_q_and_k": times["prologue"],
-            "prologue_gbs": nbytes / (times["prologue"] / 1e3) / 1e9,
-            "prologue_frac_of_hbm": nbytes / (times["prologue"] / 1e3) / 1e9 / peaks["hbm"],
-        }
-        del q, k, v, q8, k8, out
+            times = {}
+            for name, fn in (("prologue", prologue), ("attention", attn)):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(calls):
+                    fn()
+                e1.record()
+                torch.cuda.synchronize(dev)
+                times[name] = e0.elapsed_time(e1) / calls
+            tf = w.flops / times["attention"] / 1e9
+            e4m3_peak = peaks["bf16"] * (2.0 if fp8 else 4.0 / 3.0)
+            nbytes = (q.numel() + k.numel() + (v.numel() if fp8 else 0)) * 3.0
+            res[mode][w.name] = {
+                "shape": [w.B, w.H, w.Lq, w.Lk, w.d],
+                "ms_attention": times["attention"], "tflops": tf,
+                "speedup_vs_bf16_eager": bf16_ms[w.name] / times["attention"]
+                if w.name in bf16_ms else None,
+                "frac_of_bf16_peak": tf / peaks["bf16"],
+                ("frac_of_e4m3_peak" if fp8 else "frac_of_mixed_peak"): tf / e4m3_peak,
+                ("ms_prologue_q_k_v" if fp8 else "ms_prologue_q_and_k"): times["prologue"],
+                "prologue_gbs": nbytes / (times["prologue"] / 1e3) / 1e9,
+                "prologue_frac_of_hbm": nbytes / (times["prologue"] / 1e3) / 1e9 / peaks["hbm"],
+            }
+        del q, k, v, q8, k8, v8, out
         torch.cuda.empty_cache()
-    return res
+    return res["qk8"], res["fp8"]
+
+
+def v_calibration(v) -> float:
+    """Per-tensor dequantisation scale of the values, max|V| / 448 (a static
+    scale taken once, before any timed region, as a calibration pass would)."""
+    import numpy as np
+    return float(np.float32(float(v.abs().max()) / 448.0))
 
 
 def bench_ours(args):
@@ -496,18 +520,25 @@ def bench_ours(args):
     out = torch.empty_like(q)
     stream = torch.cuda.current_stream(dev)
     flops = w.flops
-    qk8 = args.path == "qk8"
+    fp8 = args.path == "fp8"
+    qk8 = args.path == "qk8" or fp8       # e4m3 queries and keys
     if qk8:
         if not w.rms_norm or w.d != 128:
-            raise SystemExit("--path qk8 needs an RMS-normalised d=128 workload")
+            raise SystemExit(f"--path {args.path} needs an RMS-normalised d=128 workload")
         # |RMS-normalised value| <= sqrt(d): 448/sqrt(d) never saturates e4m3
         s8 = float(np.float32(math.sqrt(w.d) / 448.0))
         inv8 = float(np.float32(448.0 / math.sqrt(w.d)))
         q8 = dit.rmsnorm_e4m3(q, inv8)
         k8 = dit.rmsnorm_e4m3(k, inv8)
+    if fp8:
+        vs8 = v_calibration(v)
+        inv_vs8 = float(np.float32(1.0 / vs8))
+        v8 = dit.quantize_e4m3(v, inv_vs8)
 
     def fwd():
-        if qk8:
+        if fp8:
+            dit.forward_fp8(q8, k8, v8, s8, s8, vs8, w.scale, out=out)
+        elif qk8:
             dit.forward_qk8(q8, k8, v, s8, s8, w.scale, out=out)
         else:
             dit.forward(q, k, v, w.scale, out=out)
@@ -548,6 +579,8 @@ def bench_ours(args):
         if qk8:
             bset += [torch.empty(q.shape, dtype=torch.float8_e4m3fn, device=dev),
                      torch.empty(k.shape, dtype=torch.float8_e4m3fn, device=dev)]
+        if fp8:
+            bset.append(torch.empty(v.shape, dtype=torch.float8_e4m3fn, device=dev))
         bufs.append(bset)
     s_in, s_run, s_out = (torch.cuda.Stream(dev) for _ in range(3))
     ev_in, ev_run, ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
@@ -566,7 +599,13 @@ def bench_ours(args):
             s_run.wait_event(ev_in[b])
             if used[b]:
                 s_run.wait_event(ev_out[b])         # the last read-back of this output is done
-            if qk8:
+            if fp8:
+                q8d, k8d, v8d = bufs[b][4:]
+                dit.rmsnorm_e4m3(qd, inv8, out=q8d)
+                dit.rmsnorm_e4m3(kd, inv8, out=k8d)
+                dit.quantize_e4m3(vd, inv_vs8, out=v8d)
+                dit.forward_fp8(q8d, k8d, v8d, s8, s8, vs8, w.scale, out=od)
+            elif qk8:
                 q8d, k8d = bufs[b][4:]
                 dit.rmsnorm_e4m3(qd, inv8, out=q8d)
                 dit.rmsnorm_e4m3(kd, inv8, out=k8d)
@@ -602,18 +641,23 @@ def bench_ours(args):
         return 0
 
     # the attention kernel, plus the merge kernel when the last wave is split
-    launches_per_call = 1 + int(dit.workspace_size(w.B, w.H, w.Lq, w.Lk, w.d, qk8) > 0)
+    variant = 2 if fp8 else (1 if qk8 else 0)
+    launches_per_call = 1 + int(dit.workspace_size(w.B, w.H, w.Lq, w.Lk, w.d,
+                                                   variant=variant) > 0)
     mean_launch = statistics.mean(per_launch)
     achieved = flops / (mean_launch / 1e3) / 1e12
-    traffic = recorded_traffic(w.name + ("/qk8" if qk8 else ""))
+    traffic = recorded_traffic(w.name + ("/fp8" if fp8 else "/qk8" if qk8 else ""))
     qk_bytes = 1 if qk8 else 2
-    # e4m3 S = Q K^T runs at twice the bf16 rate (nominal ratio), P V at the bf16 rate
-    peak = peaks["bf16"] * (4.0 / 3.0 if qk8 else 1.0)
+    v_bytes = 1 if fp8 else 2
+    # e4m3 products run at twice the bf16 rate (nominal ratio): S = Q K^T with
+    # qk8, both products with fp8
+    peak = peaks["bf16"] * (2.0 if fp8 else 4.0 / 3.0 if qk8 else 1.0)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3 QK^T, bf16 PV" if qk8 else "bf16",
+        "dtype": ("e4m3 QK^T and PV (e4m3 P)" if fp8 else "e4m3 QK^T, bf16 PV" if qk8
+                  else "bf16"),
         "data": "synthetic",
         "config": {"workload": w.name, "path": args.path, "B": w.B, "H": w.H, "Lq": w.Lq,
                    "Lk": w.Lk, "d": w.d, "segments": dict(w.segments), "parallelism": f"replicas x{world}",
@@ -626,24 +670,25 @@ def bench_ours(args):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peaks['source']} dense bf16 burst"
-                                    + (" x 4/3 (half the flops at the nominal 2x e4m3 rate)"
+                                    + (" x 2 (all flops at the nominal 2x e4m3 rate)" if fp8
+                                       else " x 4/3 (half the flops at the nominal 2x e4m3 rate)"
                                        if qk8 else ""),
                      "algorithmic_bytes": float((qk_bytes + 2) * w.B * w.H * w.Lq * w.d
-                                                + (qk_bytes + 2) * w.B * w.H * w.Lk * w.d),
+                                                + (qk_bytes + v_bytes) * w.B * w.H * w.Lk * w.d),
                      "kernel_source": kernel_source_hash()},
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                 "overlap": "copies of one step overlap the forward of the previous one "
                            "(two buffer sets, three streams)"},
         "gpu_launches": args.steps * launches_per_call,
-        "e2e_gpu_launches_per_step": launches_per_call + (2 if qk8 else 0),
+        "e2e_gpu_launches_per_step": launches_per_call + (3 if fp8 else 2 if qk8 else 0),
         "clocks": sampler.summary(),
     }
     if world == 1 and not args.no_sweep:
         line["per_workload"] = workload_sweep(dit, dev)
         line["rmsnorm_qk_prologue"] = rmsnorm_roofline(dit, dev, peaks)
-        line["qk8"] = qk8_sweep(dit, dev, peaks,
-                                {n: r["ms_eager"] for n, r in line["per_workload"].items()})
+        bf16_ms = {n: r["ms_eager"] for n, r in line["per_workload"].items()}
+        line["qk8"], line["fp8"] = e4m3_sweep(dit, dev, peaks, bf16_ms)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     print(json.dumps(line), flush=True)

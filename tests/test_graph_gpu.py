@@ -132,6 +132,49 @@ def test_graph_replay_e4m3_pipeline(dit):
     assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
 
 
+def test_graph_replay_fp8_pipeline(dit):
+    """The e4m3 Q/K/V path captured as one graph: RMS-norm + quantisation of
+    Q and K, quantisation of V, the e4m3 Q/K/V forward with a split tail;
+    replays must equal the eager calls bit for bit."""
+    import torch
+    rng = np.random.default_rng(24)
+    B, H, Lq, Lk, d = 1, 2, 900, 6000, 128
+    assert dit.workspace_size(B, H, Lq, Lk, d, variant=2) > 0
+    q = to_device(W.random_bf16(rng, (B, H, Lq, d)))
+    k = to_device(W.random_bf16(rng, (B, H, Lk, d)))
+    v = to_device(W.random_bf16(rng, (B, H, Lk, d)))
+    s = float(np.float32(math.sqrt(d) / 448))
+    inv = float(np.float32(448 / math.sqrt(d)))
+    vs = 0.0125
+
+    def pipeline(q8, k8, v8, out):
+        dit.rmsnorm_e4m3(q, inv, out=q8)
+        dit.rmsnorm_e4m3(k, inv, out=k8)
+        dit.quantize_e4m3(v, 1 / vs, out=v8)
+        dit.forward_fp8(q8, k8, v8, s, s, vs, out=out)
+
+    def buffers():
+        return (torch.empty_like(q, dtype=torch.float8_e4m3fn),
+                torch.empty_like(k, dtype=torch.float8_e4m3fn),
+                torch.empty_like(v, dtype=torch.float8_e4m3fn), torch.empty_like(q))
+
+    eager = buffers()
+    pipeline(*eager)
+    captured = buffers()
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(st):
+        with torch.cuda.graph(g, stream=st):
+            pipeline(*captured)
+    torch.cuda.synchronize()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(captured[2].view(torch.uint8), eager[2].view(torch.uint8))
+    assert torch.equal(captured[3].view(torch.int16), eager[3].view(torch.int16))
+
+
 def test_graph_replay_split_tail(dit):
     """A call whose work units are split over key ranges (attention kernel,
     then the merge kernel, workspace from the capture's memory pool) replays
