@@ -61,7 +61,12 @@ constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s per wait
 constexpr float kRescaleThreshold = 8.0f;          // log2 units
-constexpr float kOptimisticSumLimit = 65536.0f;    // 2^16: a tile sum above it forces the max
+// 2^48: a tile's row sum above it (or not finite) forces the max pass.  Below
+// it the stale max is kept even when the row's max has risen: O and l carry
+// the same factor, which cancels in O / l, and p <= 2^48 keeps both far from
+// fp32's range.  (At 2^16, rows whose keys include a few large outliers took
+// the max pass on about 14% of warp steps.)
+constexpr float kOptimisticSumLimit = 281474976710656.0f;
 
 template <int D>
 struct Traits {
@@ -472,8 +477,9 @@ __device__ __forceinline__ void softmax_tile_half(uint32_t taddr_s, int key0, bo
     max_pass();
   } else {
     // Optimistic pass against the running max.  If a row's rounded sum
-    // exceeds 2^16, some p > 2^9: the row raises its max (always, since
-    // p > 2^8), rescales l and O and recomputes.  Warp-uniform branch.
+    // exceeds 2^48 (or overflowed), some p > 2^41: the row raises its max
+    // (always, since p > 2^8), rescales l and O and recomputes.  Warp-uniform
+    // branch.
     chunk(0, m_used);
     tmem_wait_ld();
     chunk(1, m_used);

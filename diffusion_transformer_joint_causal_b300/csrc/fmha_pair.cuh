@@ -30,9 +30,11 @@
 // 64-byte-swizzled half.  Probabilities carry an offset of 2^3 against the
 // running max and the lazy rescale threshold is 5, so every stored p is at
 // most 448 (e4m3's largest finite value; 2^8 after a max pass) and at least
-// 2^-6 (its smallest normal) unless it is under 2^-9 of the row's largest;
-// the row sum adds the rounded values.  The per-tensor value scale is applied
-// with 1/l in the epilogue.
+// 2^-6 (its smallest normal) unless it is under 2^-9 of the row's largest.
+// The row sum adds the fp32 probabilities before their rounding (two paired
+// adds per four keys; summing the rounded values through an f16 widening took
+// 10% more cycles), so every weight carries only its own rounding error.  The
+// per-tensor value scale is applied with 1/l in the epilogue.
 #pragma once
 
 namespace dit {
@@ -350,7 +352,7 @@ __device__ __forceinline__ float rowmax_chunk(const uint32_t (&sr)[32], int key0
 }
 
 // Probabilities of 32 logits rounded to e4m3, four keys per word (key order =
-// byte order), and the sum of the rounded values added into acc.
+// byte order); their fp32 values, before the rounding, are added into acc.
 template <bool kMasked>
 __device__ __forceinline__ void probs_chunk_e4m3(const uint32_t (&sr)[32], float scale_log2,
                                                  float neg_m, int key0, int valid, uint32_t* pk,
@@ -371,7 +373,11 @@ __device__ __forceinline__ void probs_chunk_e4m3(const uint32_t (&sr)[32], float
       p2 = (key0 + i + 2 < valid) ? p2 : 0.f;
       p3 = (key0 + i + 3 < valid) ? p3 : 0.f;
     }
-    pk[i / 4] = pack_e4m3x4_sum(p0, p1, p2, p3, acc[(i / 4) & 3], acc[4 + ((i / 4) & 3)]);
+    pk[i / 4] = pack_e4m3x4(p0, p1, p2, p3);
+    const float2 s = __fadd2_rn(make_float2(p0, p1), make_float2(p2, p3));
+    const float2 a = __fadd2_rn(make_float2(acc[(i / 4) & 3], acc[4 + ((i / 4) & 3)]), s);
+    acc[(i / 4) & 3] = a.x;
+    acc[4 + ((i / 4) & 3)] = a.y;
   }
 }
 
@@ -437,10 +443,11 @@ __device__ __forceinline__ void softmax_tile_lean(uint32_t taddr_s, int key0, bo
   if (first) {
     max_pass();
   } else {
-    // Optimistic pass against the running max; a rounded row sum above 2^16
-    // means some p > 2^9: raise the max (always by more than 8), rescale l
-    // and O, recompute.  With e4m3 P a row sum of 448 or more may hide a
-    // saturated value: take the max pass.  Warp-uniform branch.
+    // Optimistic pass against the running max; a rounded row sum above 2^48
+    // (or an overflow) means some p > 2^41: raise the max (always by more
+    // than 8), rescale l and O, recompute.  With e4m3 P a row sum (of the
+    // fp32 values) of 448 or more may hide a saturated value: take the max
+    // pass.  Warp-uniform branch.
     load(0);
     probs(0, m_used);
     load(1);

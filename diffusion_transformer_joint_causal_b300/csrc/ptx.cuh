@@ -520,27 +520,13 @@ __device__ __forceinline__ void add_bf16x2_halves(float& lo_acc, float& hi_acc, 
       : "r"(w));
 }
 
-// Four non-negative fp32 -> four e4m3 bytes (round to nearest even,
-// saturating at 448), p0 in bits [7:0] .. p3 in bits [31:24]; the rounded
-// values are added to acc0 (p0 + p2) and acc1 (p1 + p3).  The e4m3 -> f16
-// widening is exact; the pairwise f16 sum is exact unless the two values'
-// exponents differ by more than 7 (then it rounds at 2^-11 relative).
-__device__ __forceinline__ uint32_t pack_e4m3x4_sum(float p0, float p1, float p2, float p3,
-                                                    float& acc0, float& acc1) {
-  uint32_t w;
-  asm("{\n\t.reg .b16 lo, hi, s0, s1;\n\t.reg .b32 flo, fhi, fs;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f32 lo, %4, %3;\n\t"
-      "cvt.rn.satfinite.e4m3x2.f32 hi, %6, %5;\n\t"
-      "mov.b32 %0, {lo, hi};\n\t"
-      "cvt.rn.f16x2.e4m3x2 flo, lo;\n\t"
-      "cvt.rn.f16x2.e4m3x2 fhi, hi;\n\t"
-      "add.rn.f16x2 fs, flo, fhi;\n\t"
-      "mov.b32 {s0, s1}, fs;\n\t"
-      "add.rn.f32.f16 %1, s0, %1;\n\t"
-      "add.rn.f32.f16 %2, s1, %2;\n\t}"
-      : "=r"(w), "+f"(acc0), "+f"(acc1)
-      : "f"(p0), "f"(p1), "f"(p2), "f"(p3));
-  return w;
+// Four fp32 -> four e4m3 bytes (round to nearest even, saturating at +-448),
+// a in bits [7:0] .. d in bits [31:24].
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  uint16_t lo, hi;   // the first operand of the conversion lands in the upper byte
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
 // Two fp32 -> packed bf16x2 (round to nearest even); lo goes to bits [15:0].

@@ -12,13 +12,6 @@
 
 namespace dit {
 
-__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
-  uint16_t lo, hi;   // the first operand of the conversion lands in the upper byte
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
-  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-}
-
 template <int D, bool kE4M3>
 __global__ void __launch_bounds__(256)
     rmsnorm_kernel(const uint4* x, void* y, const uint4* __restrict__ w, int64_t rows, float eps,

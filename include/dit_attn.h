@@ -165,12 +165,11 @@ int dit_attn_forward_qk8_ws(const void* q8, const void* k8, const void* v, void*
  * finite and >= 0, v_scale finite and > 0 with a finite reciprocal, and
  * scale*q_scale*k_scale at most 3e38 (else INVALID_ARG).  Arithmetic: both
  * products on e4m3 tensor cores with exact fp32 accumulation; every p is
- * rounded to e4m3 (relative error at most 2^-4 where p >= 2^-6, i.e. for
- * every key within 2^-9 of the row's largest weight), and the row sum adds
- * the rounded p, so the output is a convex combination of the dequantised
- * value rows.  Sizes (q8, k8, v8 counted in bytes), alignment, overlap,
- * stream and error behaviour as in dit_attn_forward; NaN codes as in
- * dit_attn_forward_qk8.
+ * rounded to e4m3 for P.V (relative error at most 2^-4 where p >= 2^-6, i.e.
+ * for every key within 2^-9 of the row's largest weight) while the row sum
+ * adds the fp32 p, so each weight carries only its own rounding error.
+ * Sizes (q8, k8, v8 counted in bytes), alignment, overlap, stream and error
+ * behaviour as in dit_attn_forward; NaN codes as in dit_attn_forward_qk8.
  */
 int dit_attn_forward_fp8(const void* q8, const void* k8, const void* v8, void* out, int B, int H,
                          int Lq, int Lk, int d, float scale, float q_scale, float k_scale,
