@@ -283,12 +283,20 @@ def oracle_sample(w, n_rows, n_threads):
     return run
 
 
+def oracle_rows_per_second(run, threads: int) -> float:
+    """Rows per second of the oracle on this host: one warm-up call (thread start,
+    first touch of the inputs), then a timed call of four rows per thread."""
+    run(threads)
+    n, t = run(4 * threads)
+    return n / max(t, 1e-6)
+
+
 def cpu_baseline(w, seconds: float):
     import oracle
     threads = oracle.default_threads()
     run = oracle_sample(w, 0, threads)
-    n1, t1 = run(threads)                       # calibration: one row per thread
-    n = max(threads, int(threads * seconds / max(t1, 1e-3)))
+    rate = oracle_rows_per_second(run, threads)
+    n = max(threads, int(rate * seconds))
     n, t = run(n)
     flops = 4.0 * w.Lk * w.d * n
     return {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
@@ -308,10 +316,10 @@ def bench_reference(args):
     w = W.workload(args.workload)
     threads = oracle.default_threads()
     run = oracle_sample(w, 0, threads)
-    n1, t1 = run(threads)
+    rate = oracle_rows_per_second(run, threads)
     # whole run within about two minutes: at most 2 s per step
     step_s = min(2.0, 120.0 / max(1, args.steps + args.warmup))
-    per_step = max(threads, int(threads * step_s / max(t1, 1e-3)))
+    per_step = max(threads, int(rate * step_s))
     for _ in range(args.warmup):
         run(per_step)
     times = []
