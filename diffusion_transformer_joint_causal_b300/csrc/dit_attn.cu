@@ -6,25 +6,32 @@
 // o_i = sum_j softmax_j(scale * q_i . k_j) v_j for every (batch, head), over
 // the joint text+image token sequence.
 //
-// Kernel structure (one persistent CTA per SM, 320 threads):
-//   warps 0-3  softmax warpgroup 0: owns query tile 0 (TMEM lanes 0..127)
-//   warps 4-7  softmax warpgroup 1: owns query tile 1
-//   warp  8    tcgen05 MMA issuer and TMEM allocator
-//   warp  9    TMA producer
+// This file holds the device pieces the kernels share (parameters, work
+// items, bounded waits, the probability and row-sum helpers, the partial-row
+// store), the single-CTA kernel that serves d = 64, and the host side of the
+// C ABI.  d = 128 runs on CTA pairs (fmha_pair.cuh: bf16, e4m3 Q/K and e4m3
+// Q/K/V variants); combine.cuh merges a split last wave; rmsnorm.cuh and
+// quantize.cuh are the input prologues.
+//
+// Single-CTA kernel (d = 64; one persistent CTA per SM, 384 threads):
+//   warps 0-7   softmax: query tile 0, then tile 1, of every key tile
+//   warp  8     tcgen05 MMA issuer and TMEM allocator
+//   warp  9     TMA producer
 //   warps 10-11 idle (they complete the third warpgroup for setmaxnreg)
 // A work unit is 2 x 128 query rows of one (b,h).  Q tiles stay in shared
 // memory for the whole unit; K and V tiles of 128 keys stream through a ring
 // of shared-memory stages.  For every key tile j the MMA warp computes
-// S_t = Q_t K_j^T into TMEM; softmax warpgroup t turns S_t into bf16
+// S_t = Q_t K_j^T into TMEM; the softmax warps turn S_t into bf16
 // probabilities P_t in place (the same TMEM columns), and the MMA warp then
-// accumulates O_t += P_t V_j in TMEM.  The two warpgroups alternate so that
-// one tile's softmax overlaps the other tile's MMAs.
+// accumulates O_t += P_t V_j in TMEM; one tile's softmax overlaps the other
+// tile's MMAs.
 //
-// Online softmax (base 2): x = s * scale*log2(e); the running maximum m is
-// only raised when a tile's maximum exceeds it by more than 8 (a factor 256),
-// and then l and O are rescaled by exp2(m_old - m_new).  Probabilities are
-// exp2(x - m) <= 256, the row sum l accumulates in fp32, and the result
-// O / l is exact in exact arithmetic whatever m is.
+// Online softmax (base 2): x = s * scale*log2(e).  Probabilities are first
+// computed against the running maximum m; only when a tile's row sum against
+// it exceeds 2^48 (or overflows) does the row take the tile's maximum, and m
+// rises only if that maximum exceeds it by more than 8 (a factor 256); l and
+// O are then rescaled by exp2(m_old - m_new).  O / l is exact in exact
+// arithmetic whatever m is.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -76,7 +83,8 @@ struct Traits {
   static constexpr uint32_t kBoxBytes = 128u * 128u;          // 128 rows x 128 bytes
   static constexpr uint32_t kTileBytes = kBoxBytes * kBoxes;  // one Q, K or V tile
   static constexpr int kStages = D == 128 ? 4 : 8;
-  // TMEM columns (fp32): S0, S1, O0, O1.  P_t (bf16 pairs) reuses S_t's first 64.
+  // TMEM columns (fp32): S0, S1, O0, O1.  P_t (bf16 pairs) reuses the first 32
+  // of each half-row's 64 S_t columns.
   __host__ __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
   __host__ __device__ static constexpr uint32_t col_o(int t) { return 256u + static_cast<uint32_t>(D) * t; }
   static constexpr uint32_t kTmemCols = 512;
@@ -974,9 +982,6 @@ int dit_attn_create(void) {
   }
   e = cudaFuncSetAttribute(dit::fmha_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Traits<64>::kSmemBytes);
-  if (e != cudaSuccess) return cuda_fail(e);
-  e = cudaFuncSetAttribute(dit::fmha_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Traits<128>::kSmemBytes);
   if (e != cudaSuccess) return cuda_fail(e);
   {
     int rc = DIT_ATTN_OK, bf16_pairs = 0, qk8_pairs = 0, fp8_pairs = 0;

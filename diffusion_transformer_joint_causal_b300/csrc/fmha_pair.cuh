@@ -467,8 +467,9 @@ __device__ __forceinline__ void softmax_tile_lean(uint32_t taddr_s, int key0, bo
   l += sum8(acc);
 }
 
-// Softmax and epilogue of the pair kernel: warp w works on query tile w / 8,
-// TMEM lanes 32*(w%4) + 16*((w/8)... two threads per row as in softmax_role.
+// Softmax and epilogue of the pair kernel: warp w works on query tile w / 8
+// and, with q = w mod 8, on TMEM lanes (rows) 32*(q%4) + 16*(q/4) .. +15, two
+// threads per row (lanes 0-15 take keys 0-63, lanes 16-31 keys 64-127).
 // Each warp arrives once per key tile on its tile's P-ready barrier of the
 // leader CTA (8 warps x 2 CTAs).
 template <int D, class T>
