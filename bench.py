@@ -274,12 +274,15 @@ def oracle_sample(w, n_rows, n_threads):
     order = np.random.default_rng(0).permutation(len(rows))
     bh, rows = bh[order], rows[order]
 
-    def run(n):
-        n = min(n, len(rows))
+    def run(n, start=0):
+        n = max(0, min(n, len(rows) - start))
         t0 = time.perf_counter()
-        oracle.attention_rows(q, k, v, w.scale, bh[:n], rows[:n], n_threads=n_threads)
+        if n:
+            oracle.attention_rows(q, k, v, w.scale, bh[start:start + n], rows[start:start + n],
+                                  n_threads=n_threads)
         return n, time.perf_counter() - t0
 
+    run.total = len(rows)
     return run
 
 
@@ -292,12 +295,21 @@ def oracle_rows_per_second(run, threads: int) -> float:
 
 
 def cpu_baseline(w, seconds: float):
+    """The oracle on consecutive chunks of the workload's sampled rows until
+    about `seconds` of work (or the sample) is done; each chunk is sized from
+    the rate measured so far."""
     import oracle
     threads = oracle.default_threads()
     run = oracle_sample(w, 0, threads)
     rate = oracle_rows_per_second(run, threads)
-    n = max(threads, int(rate * seconds))
-    n, t = run(n)
+    n, t, start = 0, 0.0, 0
+    while t < seconds and start < run.total:
+        want = max(threads, int(rate * (seconds - t)))
+        k, dt = run(want, start)
+        start += k
+        n += k
+        t += dt
+        rate = n / max(t, 1e-6)
     flops = 4.0 * w.Lk * w.d * n
     return {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": f"{n} query rows of {w.name} (seeded 256-row samples per (b,h)), "
