@@ -317,3 +317,24 @@ def test_quantize_then_forward_fp8(dit):
     assert np.array_equal(v8.view(torch.uint8).cpu().numpy(), vc)
     check_full(got, qd.astype(np.float64) * s, kd.astype(np.float64) * s,
                W.e4m3_to_f32(vc).astype(np.float64) * vs, w.scale, "quantise + forward_fp8")
+
+
+def test_million_key_rows_fp8(dit):
+    # e4m3 Q/K/V over 2^20 + 77 keys (8193 key tiles, the split tail in 16
+    # chunks whose partial row sums carry 1 / v_scale), every eighth row.
+    B, H, Lq, Lk, d = 1, 1, 300, (1 << 20) + 77, 128
+    assert dit.workspace_size(B, H, Lq, Lk, d, variant=2) > 0
+    rng = np.random.default_rng(2401)
+    rms = lambda x: x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + np.float32(1e-6))
+    q8, qs = W.quantize_e4m3(rms(rng.standard_normal((B, H, Lq, d), dtype=np.float32)))
+    k8, ks = W.quantize_e4m3(rms(rng.standard_normal((B, H, Lk, d), dtype=np.float32)))
+    v8, vs = W.quantize_e4m3(rng.standard_normal((B, H, Lk, d), dtype=np.float32))
+    scale = float(np.float32(1 / math.sqrt(d)))
+    got = to_host_f64(run_fp8(dit, q8, k8, v8, qs, ks, vs, scale))
+    dq = lambda c, s: W.e4m3_to_f32(c).astype(np.float64) * s
+    rows = np.concatenate([np.arange(0, Lq, 8), [Lq - 1]])
+    bh = np.zeros_like(rows)
+    qd, kd, vd = dq(q8, qs), dq(k8, ks), dq(v8, vs)
+    want = oracle.attention_rows(qd, kd, vd, scale, bh, rows)
+    wabs = oracle.attention_rows(qd, kd, np.abs(vd), scale, bh, rows)
+    assert_fp8_close(got[0, 0][rows], want, wabs, "2^20 keys, e4m3")

@@ -285,3 +285,27 @@ def test_many_heads_short_rows(dit):
     rows = np.tile(np.array([0, 1, 127, 128, 255, 256, 298, 299]), B * H)
     flat = got.reshape(B * H, Lq, d)[bh, rows]
     assert_close(flat, oracle_sampled(q, k, v, scale, bh, rows), "many heads")
+
+
+def _rms_bf16(rng, shape):
+    x = rng.standard_normal(shape, dtype=np.float32)
+    x /= np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + np.float32(1e-6))
+    return W.bf16_bits(x)
+
+
+def test_million_key_rows(dit):
+    # Rows over 2^20 + 77 keys (8193 key tiles, the last ragged) with the
+    # 2048px workloads' RMS-normalised queries and keys: one work unit, whose
+    # key range the split tail cuts into 16 chunks; the fp32 row sums and the
+    # merge of the chunks are checked on every eighth query row.
+    B, H, Lq, Lk, d = 1, 1, 300, (1 << 20) + 77, 128
+    assert dit.workspace_size(B, H, Lq, Lk, d) > 0
+    rng = np.random.default_rng(2400)
+    q = _rms_bf16(rng, (B, H, Lq, d))
+    k = _rms_bf16(rng, (B, H, Lk, d))
+    v = W.random_bf16(rng, (B, H, Lk, d))
+    scale = float(np.float32(1 / math.sqrt(d)))
+    got = to_host_f64(run(dit, q, k, v, scale))
+    rows = np.concatenate([np.arange(0, Lq, 8), [Lq - 1]])
+    bh = np.zeros_like(rows)
+    assert_close(got[0, 0][rows], oracle_sampled(q, k, v, scale, bh, rows), "2^20 keys")
