@@ -274,12 +274,12 @@ def oracle_sample(w, n_rows, n_threads):
     order = np.random.default_rng(0).permutation(len(rows))
     bh, rows = bh[order], rows[order]
 
-    def run(n, start=0):
+    def run(n, start=0, threads=None):
         n = max(0, min(n, len(rows) - start))
         t0 = time.perf_counter()
         if n:
             oracle.attention_rows(q, k, v, w.scale, bh[start:start + n], rows[start:start + n],
-                                  n_threads=n_threads)
+                                  n_threads=threads or n_threads)
         return n, time.perf_counter() - t0
 
     run.total = len(rows)
@@ -311,9 +311,14 @@ def cpu_baseline(w, seconds: float):
         t += dt
         rate = n / max(t, 1e-6)
     flops = 4.0 * w.Lk * w.d * n
+    # one thread on a short sample of the same rows (about a second)
+    n1 = max(4, min(64, int(2.0 * rate / threads)))
+    n1, t1 = run(n1, 0, threads=1)
     return {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": f"{n} query rows of {w.name} (seeded 256-row samples per (b,h)), "
-                      f"FP64 C loop, {t:.1f} s"}
+                      f"FP64 C loop, {t:.1f} s",
+            "s_per_row": t / n, "s_per_row_one_thread": t1 / n1,
+            "one_thread_sample_rows": n1}
 
 
 def bench_reference(args):
