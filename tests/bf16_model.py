@@ -26,12 +26,13 @@ def bf16_round(x: np.ndarray) -> np.ndarray:
 
 
 def forward(s: np.ndarray, v: np.ndarray, rounded_sum: bool = True, tau: float = 8.0,
-            limit: float = 2.0 ** 48, bn: int = 128) -> np.ndarray:
+            limit: float = 2.0 ** 48, bn: int = 128, stats: dict | None = None) -> np.ndarray:
     x = s / math.log(2.0)
     R, L = x.shape
     m = np.full(R, -np.inf)
     l = np.zeros(R)
     O = np.zeros((R, v.shape[1]))
+    redo_rows = 0
     for j0 in range(0, L, bn):
         xt = x[:, j0:j0 + bn]
         if j0 == 0:
@@ -41,6 +42,7 @@ def forward(s: np.ndarray, v: np.ndarray, rounded_sum: bool = True, tau: float =
             pr = np.exp2(xt - m[:, None])
             redo = ~(bf16_round(pr).sum(1) <= limit)
             if redo.any():
+                redo_rows += int(redo.sum())
                 mt = xt.max(1)
                 grow = redo & (mt > m + tau)
                 f = np.where(grow, np.exp2(m - mt), 1.0)
@@ -51,4 +53,7 @@ def forward(s: np.ndarray, v: np.ndarray, rounded_sum: bool = True, tau: float =
         pb = bf16_round(pr)
         l += (pb if rounded_sum else pr).sum(1)
         O += pb @ v[j0:j0 + bn]
+    if stats is not None:
+        stats["redo_rows"] = redo_rows
+        stats["row_tiles"] = R * max(0, (L + bn - 1) // bn - 1)
     return bf16_round(O / l[:, None])

@@ -35,3 +35,29 @@ def test_rounded_row_sum_meets_the_bar_where_the_unrounded_one_does_not():
         assert np.linalg.norm(rounded - ref) / np.linalg.norm(ref) <= 5e-3
     assert worst_rounded <= 1.5e-2
     assert worst_unrounded > 2e-2
+
+
+def test_optimistic_limit_2_pow_48_removes_the_max_passes():
+    # With the optimistic limit at 2^16 the outlier keys send about one row
+    # tile in a hundred into the max pass (a warp takes it when any of its 16
+    # rows does: about one warp step in seven); at 2^48 none go, and the
+    # output stays as close to the definition (the stale max cancels in
+    # O / l; only the grid on which p is rounded to bf16 differs).
+    w = W.workload("ragged_outliers")
+    Q, K, V = W.make_qkv(w)
+    h = 12
+    rows = W.sample_rows(w, 0, h)
+    q = W.bf16_to_f32(Q)[0, h][rows].astype(np.float64)
+    k = W.bf16_to_f32(K)[0, h].astype(np.float64)
+    v = W.bf16_to_f32(V)[0, h].astype(np.float64)
+    s = w.scale * q @ k.T
+    st16, st48 = {}, {}
+    o16 = M.forward(s, v, limit=2.0 ** 16, stats=st16)
+    o48 = M.forward(s, v, limit=2.0 ** 48, stats=st48)
+    share16 = st16["redo_rows"] / st16["row_tiles"]
+    share48 = st48["redo_rows"] / st48["row_tiles"]
+    assert share16 > 0.005 and share48 < 0.1 * share16
+    ref = oracle.attention_rows(Q, K, V, w.scale, np.full(rows.shape, h), rows)
+    for o in (o16, o48):
+        assert float(np.abs(o - ref).max()) <= 1.5e-2
+        assert np.linalg.norm(o - ref) / np.linalg.norm(ref) <= 5e-3
