@@ -21,6 +21,8 @@
  *   k, v: device pointers, bf16, contiguous [B, H, Lk, d]
  *   out : device pointer, bf16, contiguous [B, H, Lq, d]; written, never read
  * Every pointer must be 16-byte aligned; out must not overlap q, k or v.
+ * (The e4m3 entry points below take one-byte e4m3 codes for q and k, or for
+ * q, k and v, with per-tensor scales.)
  * d must be 64 or 128.  Arithmetic: bf16 tensor-core products with fp32
  * accumulation, fp32 online softmax, probabilities rounded to bf16 before the
  * P.V product, output rounded to nearest-even bf16.
