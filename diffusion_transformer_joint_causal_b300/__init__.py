@@ -33,7 +33,7 @@ __all__ = ["create", "destroy", "forward", "forward_ptr", "status_string", "get_
            "rmsnorm_e4m3", "rmsnorm_e4m3_ptr", "forward_ws_ptr", "forward_qk8_ws_ptr",
            "workspace_size", "forward_noalloc", "forward_noalloc_ptr", "forward_fp8",
            "forward_fp8_ptr", "forward_fp8_ws_ptr", "quantize_e4m3", "quantize_e4m3_ptr",
-           "last_cuda_error", "version", "library_path", "DitAttnError", "STATUS",
+           "check_exp2", "forward_qnorm", "forward_qnorm_ptr", "last_cuda_error", "version", "library_path", "DitAttnError", "STATUS",
            "EXPORTED_SYMBOLS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -50,7 +50,8 @@ EXPORTED_SYMBOLS = ("dit_attn_version", "dit_attn_create", "dit_attn_forward",
                     "dit_attn_forward_qk8", "dit_attn_rmsnorm_e4m3", "dit_attn_forward_ws",
                     "dit_attn_forward_qk8_ws", "dit_attn_workspace_size",
                     "dit_attn_forward_noalloc", "dit_attn_forward_fp8",
-                    "dit_attn_forward_fp8_ws", "dit_attn_quantize_e4m3")
+                    "dit_attn_forward_fp8_ws", "dit_attn_quantize_e4m3", "dit_attn_check_exp2",
+                    "dit_attn_forward_qnorm")
 
 _lock = threading.Lock()
 _lib = None
@@ -125,6 +126,12 @@ def _load():
                                                     ctypes.c_longlong, vp]
             lib.dit_attn_quantize_e4m3.restype = c_int
             lib.dit_attn_quantize_e4m3.argtypes = [vp, vp, ctypes.c_longlong, ctypes.c_float, vp]
+            lib.dit_attn_forward_qnorm.restype = c_int
+            lib.dit_attn_forward_qnorm.argtypes = [vp, vp, vp, vp, c_int, c_int, c_int, c_int,
+                                                   c_int, ctypes.c_float, vp, ctypes.c_float, vp,
+                                                   ctypes.c_longlong, vp]
+            lib.dit_attn_check_exp2.restype = c_int
+            lib.dit_attn_check_exp2.argtypes = [vp, vp, vp, ctypes.c_longlong, c_int, vp]
             lib.dit_attn_last_cuda_error.restype = c_int
             lib.dit_attn_last_cuda_error.argtypes = []
             _lib = lib
@@ -174,6 +181,25 @@ def check_wait_timeout(limit_us: int, stream=None) -> int:
     return _load().dit_attn_check_wait_timeout(int(limit_us), _stream_handle(stream))
 
 
+def check_exp2(x, degree: int, stream=None):
+    """(y_fma, y_mufu) for a float32 CUDA tensor x: the softmax's FMA-pipe 2^x of
+    the given degree (2 or 3) and the MUFU ex2.approx it stands in for."""
+    import torch
+    if not isinstance(x, torch.Tensor) or x.dtype != torch.float32 or not x.is_cuda:
+        raise TypeError("x must be a float32 CUDA tensor")
+    x = x.contiguous()
+    y_fma, y_mufu = torch.empty_like(x), torch.empty_like(x)
+    with torch.cuda.device(x.device):
+        rc = _load().dit_attn_check_exp2(ctypes.c_void_p(x.data_ptr()),
+                                         ctypes.c_void_p(y_fma.data_ptr()),
+                                         ctypes.c_void_p(y_mufu.data_ptr()),
+                                         ctypes.c_longlong(x.numel()), int(degree),
+                                         _stream_handle(stream))
+    if rc:
+        raise DitAttnError(rc, "dit_attn_check_exp2")
+    return y_fma, y_mufu
+
+
 def forward_ptr(q: int, k: int, v: int, out: int, B: int, H: int, Lq: int, Lk: int, d: int,
                 scale: float, stream=0) -> int:
     """Raw C-ABI call with integer device pointers; returns the status code."""
@@ -213,7 +239,8 @@ def _out_like(out, q, shape):
 def workspace_size(B: int, H: int, Lq: int, Lk: int, d: int, qk8: bool = False,
                    variant: int | None = None) -> int:
     """Bytes of split-tail workspace the forward uses for these sizes (0: none).
-    variant: 0 forward, 1 forward_qk8, 2 forward_fp8 (default: 1 if qk8 else 0)."""
+    variant: 0 forward, 1 forward_qk8, 2 forward_fp8, 3 forward_qnorm
+    (default: 1 if qk8 else 0)."""
     if variant is None:
         variant = 1 if qk8 else 0
     nb = ctypes.c_longlong(0)
@@ -285,6 +312,42 @@ def forward(q, k, v, scale: float | None = None, out=None, stream=None, workspac
                             _stream_handle(stream))
     if rc:
         raise DitAttnError(rc, "dit_attn_forward_ws")
+    return out
+
+
+def forward_qnorm_ptr(q: int, k: int, v: int, out: int, B: int, H: int, Lq: int, Lk: int, d: int,
+                      scale: float, q_weight: int, eps: float, workspace: int,
+                      workspace_bytes: int, stream=0) -> int:
+    """Raw C-ABI call of dit_attn_forward_qnorm with integer device pointers."""
+    s = stream if isinstance(stream, ctypes.c_void_p) else ctypes.c_void_p(int(stream))
+    return _load().dit_attn_forward_qnorm(ctypes.c_void_p(q), ctypes.c_void_p(k),
+                                          ctypes.c_void_p(v), ctypes.c_void_p(out), B, H, Lq, Lk,
+                                          d, ctypes.c_float(scale),
+                                          ctypes.c_void_p(q_weight) if q_weight else None,
+                                          ctypes.c_float(eps), ctypes.c_void_p(workspace),
+                                          ctypes.c_longlong(workspace_bytes), s)
+
+
+def forward_qnorm(q, k, v, scale: float | None = None, q_weight=None, eps: float = 1e-6,
+                  out=None, stream=None, workspace="auto"):
+    """forward(rmsnorm(q, q_weight, eps), k, v, scale) with the query normalisation
+    inside the attention kernel (bit for bit the two-call result); d = 128."""
+    import torch
+    B, H, Lq, Lk, d = _check_qkv(q, k, v, (torch.bfloat16,))
+    out = _out_like(out, q, (B, H, Lq, d))
+    if q_weight is not None and (q_weight.dtype != torch.bfloat16 or tuple(q_weight.shape) != (d,)
+                                 or not q_weight.is_contiguous() or q_weight.device != q.device):
+        raise ValueError("q_weight must be a contiguous bf16 [d] tensor on q's device")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    with torch.cuda.device(q.device):
+        ws, ws_ptr, ws_bytes = _workspace(workspace, q.device, B, H, Lq, Lk, d, 3, stream)
+        rc = forward_qnorm_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, Lq,
+                               Lk, d, float(scale),
+                               q_weight.data_ptr() if q_weight is not None else 0, float(eps),
+                               ws_ptr, ws_bytes, _stream_handle(stream))
+    if rc:
+        raise DitAttnError(rc, "dit_attn_forward_qnorm")
     return out
 
 

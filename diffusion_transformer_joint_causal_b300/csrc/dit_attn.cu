@@ -37,6 +37,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <cfloat>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -74,6 +75,23 @@ constexpr float kRescaleThreshold = 8.0f;          // log2 units
 // fp32's range.  (At 2^16, rows whose keys include a few large outliers took
 // the max pass on about 14% of warp steps.)
 constexpr float kOptimisticSumLimit = 281474976710656.0f;
+// Which exponentials of a 32-key chunk the softmax evaluates on the FMA pipe
+// (exp2_fma_pair) instead of the MUFU unit: bit i of the bf16 mask is the key
+// pair 2i, 2i+1 (degree-3 polynomial, below bf16's rounding); bit i of the
+// e4m3 mask is the key quad 4i .. 4i+3 (degree 2, below e4m3's rounding).
+constexpr uint32_t kExp2FmaPairsBf16 = 0x0000u;
+constexpr uint32_t kExp2FmaQuadsE4M3 = 0x00u;
+
+// Words of a kernel's small "misc" area in shared memory.
+constexpr int kMiscTmem = 0;     // TMEM base address written by the allocation
+constexpr int kMiscAbort = 1;    // non-zero once any role gave up
+// Pair kernel, leader CTA only: the copies each producer issued (K/V fills,
+// query tiles 0 and 1), the leader's own and the peer's, for the teardown drain.
+constexpr int kMiscFills = 2;
+constexpr int kMiscQLoads = 3;
+constexpr int kMiscPeerFills = 5;
+constexpr int kMiscPeerQLoads = 6;
+constexpr int kMiscWords = 8;
 
 template <int D>
 struct Traits {
@@ -103,7 +121,7 @@ struct Traits {
   static constexpr int kBarDrain = kBarOFull + 2;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr uint32_t kSmemBytes = 1024 + kOffMisc + 16;
+  static constexpr uint32_t kSmemBytes = 1024 + kOffMisc + kMiscWords * 4;
 };
 
 struct Params {
@@ -123,6 +141,8 @@ struct Params {
   float* part_ml;    // [chunk][512 rows][2] fp32: running max (log2 units), row sum
   float v_scale;     // e4m3 values: dequantisation scale of v (1 otherwise)
   float inv_v_scale; // 1 / v_scale
+  const __nv_bfloat16* q_weight;   // fused query RMS norm: weight [128] or null
+  float q_eps;                     // fused query RMS norm: epsilon
 };
 
 // One work item: query block `qblock` of head `bh` against key tiles
@@ -153,7 +173,9 @@ struct Shared {
   uint32_t base;          // shared-window address of the aligned base
   uint32_t bar0;          // address of barrier 0
   volatile int* abort;    // set when any role gives up
+  uint32_t misc;          // shared-window address of the misc words (kMisc*)
   __device__ uint32_t bar(int i) const { return bar0 + 8u * static_cast<uint32_t>(i); }
+  __device__ uint32_t misc_word(int i) const { return misc + 4u * static_cast<uint32_t>(i); }
 };
 
 // Give up: stop every role of this CTA (and, for a CTA pair, of the peer CTA)
@@ -398,8 +420,15 @@ __device__ __forceinline__ void probs_chunk(const uint32_t (&sr)[32], float scal
   for (int i = 0; i < 32; i += 2) {
     const float2 x =
         __ffma2_rn(make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), sl2, nm);
-    float p0 = ex2_approx(x.x);
-    float p1 = ex2_approx(x.y);
+    float p0, p1;
+    if ((kExp2FmaPairsBf16 >> (i / 2)) & 1u) {   // this pair's exp2 on the FMA pipe
+      const float2 e = exp2_fma_pair<3>(x);
+      p0 = e.x;
+      p1 = e.y;
+    } else {
+      p0 = ex2_approx(x.x);
+      p1 = ex2_approx(x.y);
+    }
     if (kMasked) {
       p0 = (key0 + i < valid) ? p0 : 0.f;
       p1 = (key0 + i + 1 < valid) ? p1 : 0.f;
@@ -414,23 +443,33 @@ __device__ __forceinline__ float sum8(const float (&acc)[8]) {
   return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
 }
 
+// Largest scaled logit s * scale_log2 of a half-row's 64 logits, keys at or
+// beyond `valid` excluded (-inf when all are): scale_log2 times the largest
+// raw logit when scale_log2 >= 0, times the smallest when it is negative (the
+// sign is the same for the whole launch).
 template <bool kMasked>
-__device__ __forceinline__ float rowmax_half(const uint32_t (&sr)[2][32], int key0, int valid) {
+__device__ __forceinline__ float rowmax_half(const uint32_t (&sr)[2][32], int key0, int valid,
+                                             float scale_log2) {
+  const bool neg = scale_log2 < 0.f;
+  const float sentinel = neg ? INFINITY : -INFINITY;
   float m[8];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) m[k] = -INFINITY;
+  for (int k = 0; k < 8; ++k) m[k] = sentinel;
 #pragma unroll
   for (int c = 0; c < 2; ++c)
 #pragma unroll
     for (int i = 0; i < 32; i += 2) {
       float a = __uint_as_float(sr[c][i]), b = __uint_as_float(sr[c][i + 1]);
       if (kMasked) {
-        a = (key0 + c * 32 + i < valid) ? a : -INFINITY;
-        b = (key0 + c * 32 + i + 1 < valid) ? b : -INFINITY;
+        a = (key0 + c * 32 + i < valid) ? a : sentinel;
+        b = (key0 + c * 32 + i + 1 < valid) ? b : sentinel;
       }
-      m[(c * 16 + i / 2) & 7] = fmax3(m[(c * 16 + i / 2) & 7], a, b);
+      m[(c * 16 + i / 2) & 7] = neg ? fmin3(m[(c * 16 + i / 2) & 7], a, b)
+                                    : fmax3(m[(c * 16 + i / 2) & 7], a, b);
     }
-  return fmaxf(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], fmax3(m[5], m[6], m[7])));
+  const float e = neg ? fminf(fmin3(m[0], m[1], m[2]), fmin3(m[3], m[4], fmin3(m[5], m[6], m[7])))
+                      : fmaxf(fmax3(m[0], m[1], m[2]), fmax3(m[3], m[4], fmax3(m[5], m[6], m[7])));
+  return e == sentinel ? -INFINITY : e * scale_log2;
 }
 
 // One query tile's softmax step for this thread's half-row (keys key0 ..
@@ -465,9 +504,9 @@ __device__ __forceinline__ void softmax_tile_half(uint32_t taddr_s, int key0, bo
   // (first tile, or a recompute).
   auto max_pass = [&]() {
     tmem_wait_st();   // earlier optimistic P stores land before they are overwritten
-    float mx = masked ? rowmax_half<true>(sr, key0, valid) : rowmax_half<false>(sr, key0, kBN);
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-    const float m_tile = mx * scale_log2;
+    const float mx = masked ? rowmax_half<true>(sr, key0, valid, scale_log2)
+                            : rowmax_half<false>(sr, key0, kBN, scale_log2);
+    const float m_tile = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
     float factor = 1.f;
     if (m_tile > m_used + kRescaleThreshold) {
       factor = ex2_approx(m_used - m_tile);   // 0 on the first tile
@@ -604,11 +643,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
-  uint32_t* misc = reinterpret_cast<uint32_t*>(base_ptr + T::kOffMisc);  // [0] TMEM address, [1] abort
+  uint32_t* misc = reinterpret_cast<uint32_t*>(base_ptr + T::kOffMisc);
   Shared sh;
   sh.base = base;
   sh.bar0 = base + T::kOffBar;
-  sh.abort = reinterpret_cast<volatile int*>(misc + 1);
+  sh.abort = reinterpret_cast<volatile int*>(misc + kMiscAbort);
+  sh.misc = base + T::kOffMisc;
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
 
@@ -634,13 +674,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     tma_prefetch_desc(&tmV);
   }
   if (warp == kMmaWarp) {
-    tmem_alloc(smem_u32(misc), T::kTmemCols);
+    tmem_alloc(smem_u32(misc + kMiscTmem), T::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = misc[0];
+  const uint32_t tmem = misc[kMiscTmem];
 
   if (warp < kMmaWarp) {
     reg_alloc<kRegsSoftmax>();
@@ -680,6 +720,23 @@ __global__ void wait_timeout_kernel(uint64_t limit_ns) {
   }
 }
 
+// Self-test of the FMA-pipe exp2: y_fma[i] = exp2_fma_pair of x[i] (degree 2
+// or 3), y_mufu[i] = ex2.approx.ftz of x[i], one element per thread.
+template <int kDeg>
+__global__ void exp2_check_kernel(const float* __restrict__ x, float* __restrict__ y_fma,
+                                  float* __restrict__ y_mufu, int64_t n) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const float v = x[i];
+  y_fma[i] = exp2_fma_pair<kDeg>(make_float2(v, v)).x;
+  y_mufu[i] = ex2_approx(v);
+}
+
+// Read and clear the device error word in one atomic step, so that a TIMEOUT
+// a kernel on another stream records meanwhile is never lost.
+__device__ int g_error_taken = 0;
+__global__ void take_device_error_kernel() { g_error_taken = atomicExch(&g_device_error, 0); }
+
 }  // namespace dit
 
 #include "fmha_pair.cuh"
@@ -692,16 +749,29 @@ namespace {
 
 using dit::Traits;
 
+// Scratch of dit_attn_forward_noalloc, a file-scope device array: room for the
+// split tail's partial rows (512 x (128 + 2) fp32 per key-range chunk) of up
+// to kScratchChunks chunks.  A split plan needs at most one chunk per CTA pair
+// (74 on a 148-SM B300).  In host code g_scratch only names the array; its
+// device address comes from cudaGetSymbolAddress in dit_attn_create.
+constexpr int64_t kScratchChunks = 80;
+constexpr int64_t kScratchBytes =
+    kScratchChunks * 2 * dit::kUnitRows * (128 + 2) * static_cast<int64_t>(sizeof(float));
+static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
+
 struct DeviceState {
   bool ready = false;
   int num_sms = 0;
   int max_pairs = 0;       // co-resident clusters of two CTAs of the bf16 pair kernel
   int max_pairs_qk8 = 0;   // the same for the e4m3-QK pair kernel
   int max_pairs_fp8 = 0;   // the same for the e4m3 Q/K/V pair kernel
+  int max_pairs_qnorm = 0; // the same for the bf16 pair kernel with the fused query norm
+  void* scratch = nullptr; // device address of g_scratch on this device
 };
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
+std::mutex g_err_mu;   // serialises dit_attn_get_device_error
 DeviceState g_state[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 thread_local int g_last_cuda_error = 0;
@@ -774,6 +844,8 @@ int launch(const void* q, const void* k, const void* v, void* out, int64_t BH, i
   p.part_ml = nullptr;
   p.v_scale = 1.f;
   p.inv_v_scale = 1.f;
+  p.q_weight = nullptr;
+  p.q_eps = 0.f;
   const int grid = p.num_units < num_sms ? p.num_units : num_sms;
   dit::fmha_fwd_kernel<D><<<grid, dit::kNumThreads, Traits<D>::kSmemBytes, stream>>>(tq, tk, tv, p);
   const cudaError_t e = cudaGetLastError();
@@ -833,10 +905,12 @@ SplitPlan plan_split(int64_t num_units, int n_kv, int max_pairs) {
 // scales; with kPV8, v holds e4m3 bytes too, dequantised by v_scale.  With a
 // workspace of at least the plan's size the last, partial wave runs split,
 // followed by the combine kernel on the same stream.
-template <bool kQK8, bool kPV8>
+// With kNormQ, q holds un-normalised bf16 queries that the kernel RMS-normalises
+// (weight q_weight or none, epsilon q_eps) before their first product.
+template <bool kQK8, bool kPV8, bool kNormQ = false>
 int launch_pair(const void* q, const void* k, const void* v, void* out, int64_t BH, int Lq, int Lk,
                 double scale, cudaStream_t stream, int max_pairs, void* ws, int64_t ws_bytes,
-                float v_scale = 1.f) {
+                float v_scale = 1.f, const void* q_weight = nullptr, float q_eps = 0.f) {
   CUtensorMap tq, tk, tv;
   int rc;
   const int qk_bytes = kQK8 ? 1 : 2;
@@ -855,6 +929,8 @@ int launch_pair(const void* q, const void* k, const void* v, void* out, int64_t 
   p.scale_log2 = static_cast<float>(scale * 1.4426950408889634);
   p.v_scale = v_scale;
   p.inv_v_scale = 1.f / v_scale;
+  p.q_weight = static_cast<const __nv_bfloat16*>(q_weight);
+  p.q_eps = q_eps;
   SplitPlan plan = plan_split(p.num_units, (Lk + dit::kBN - 1) / dit::kBN, max_pairs);
   if (plan.splits > 1 && (!ws || ws_bytes < plan.ws_bytes))
     plan = SplitPlan{p.num_units, 1, p.num_units, 0, 0};
@@ -867,7 +943,8 @@ int launch_pair(const void* q, const void* k, const void* v, void* out, int64_t 
   cudaLaunchAttribute attr;
   cudaLaunchConfig_t cfg =
       pair_launch_config(2 * pairs, stream, &attr, dit::PairTraitsT<kQK8, kPV8>::kSmemBytes);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, dit::fmha_fwd_pair_kernel<kQK8, kPV8>, tq, tk, tv, p);
+  cudaError_t e =
+      cudaLaunchKernelEx(&cfg, dit::fmha_fwd_pair_kernel<kQK8, kPV8, kNormQ>, tq, tk, tv, p);
   if (e != cudaSuccess) return cuda_fail(e);
   if (plan.splits > 1) {
     const int64_t rows = (plan.num_items - plan.split_base) / plan.splits * int64_t{kPairUnitRows};
@@ -882,23 +959,28 @@ int launch_pair(const void* q, const void* k, const void* v, void* out, int64_t 
 
 // Shared memory and cluster attributes of a pair kernel; *pairs = clusters of
 // two that fit on the device at once.
-template <bool kQK8, bool kPV8>
+template <bool kQK8, bool kPV8, bool kNormQ = false>
 int setup_pair_kernel(int num_sms, int* pairs) {
   const uint32_t smem = dit::PairTraitsT<kQK8, kPV8>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(dit::fmha_fwd_pair_kernel<kQK8, kPV8>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto* kernel = dit::fmha_fwd_pair_kernel<kQK8, kPV8, kNormQ>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e);
-  e = cudaFuncSetAttribute(dit::fmha_fwd_pair_kernel<kQK8, kPV8>,
-                           cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
   if (e != cudaSuccess) return cuda_fail(e);
   cudaLaunchAttribute attr;
   cudaLaunchConfig_t cfg = pair_launch_config(num_sms, nullptr, &attr, smem);
   int clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&clusters, dit::fmha_fwd_pair_kernel<kQK8, kPV8>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
   if (e != cudaSuccess) return cuda_fail(e);
   if (clusters < 1) return cuda_fail(cudaErrorInvalidConfiguration);
   *pairs = clusters;
   return DIT_ATTN_OK;
+}
+
+// A logit scale is usable when it is finite and scale * log2(e), the factor the
+// kernels apply in fp32, is finite too (|scale| <= 2.35e38); any sign.
+bool logit_scale_ok(double scale) {
+  return std::isfinite(scale) && std::fabs(scale * 1.4426950408889634) <= FLT_MAX;
 }
 
 // Argument checks shared by the bf16 and e4m3 forwards (qk_bytes, v_bytes =
@@ -907,7 +989,7 @@ int check_forward_args(const void* q, const void* k, const void* v, const void* 
                        int Lq, int Lk, int d, float scale, int qk_bytes, int v_bytes = 2) {
   if (!q || !k || !v || !out) return DIT_ATTN_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || Lq < 1 || Lk < 1) return DIT_ATTN_ERR_INVALID_ARG;
-  if (!std::isfinite(scale) || scale < 0.f) return DIT_ATTN_ERR_INVALID_ARG;
+  if (!logit_scale_ok(scale)) return DIT_ATTN_ERR_INVALID_ARG;
   const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
                         reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out);
   if (mis & 15u) return DIT_ATTN_ERR_INVALID_ARG;
@@ -984,16 +1066,27 @@ int dit_attn_create(void) {
                            Traits<64>::kSmemBytes);
   if (e != cudaSuccess) return cuda_fail(e);
   {
-    int rc = DIT_ATTN_OK, bf16_pairs = 0, qk8_pairs = 0, fp8_pairs = 0;
+    int rc = DIT_ATTN_OK, bf16_pairs = 0, qk8_pairs = 0, fp8_pairs = 0, qnorm_pairs = 0;
     if ((rc = setup_pair_kernel<false, false>(prop.multiProcessorCount, &bf16_pairs)) != DIT_ATTN_OK)
       return rc;
     if ((rc = setup_pair_kernel<true, false>(prop.multiProcessorCount, &qk8_pairs)) != DIT_ATTN_OK)
       return rc;
     if ((rc = setup_pair_kernel<true, true>(prop.multiProcessorCount, &fp8_pairs)) != DIT_ATTN_OK)
       return rc;
+    if ((rc = setup_pair_kernel<false, false, true>(prop.multiProcessorCount, &qnorm_pairs)) !=
+        DIT_ATTN_OK)
+      return rc;
     g_state[dev].max_pairs = bf16_pairs;
+    g_state[dev].max_pairs_qnorm = qnorm_pairs;
     g_state[dev].max_pairs_qk8 = qk8_pairs;
     g_state[dev].max_pairs_fp8 = fp8_pairs;
+  }
+  {
+    // the no-allocation forward's scratch: its device address on this device
+    void* scratch = nullptr;
+    e = cudaGetSymbolAddress(&scratch, g_scratch);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_state[dev].scratch = scratch;
   }
   g_state[dev].num_sms = prop.multiProcessorCount;
   g_state[dev].ready = true;
@@ -1045,7 +1138,7 @@ int dit_attn_forward_qk8_ws(const void* q8, const void* k8, const void* v, void*
   if (!std::isfinite(q_scale) || !std::isfinite(k_scale) || q_scale < 0.f || k_scale < 0.f)
     return DIT_ATTN_ERR_INVALID_ARG;
   const double logit_scale = static_cast<double>(scale) * q_scale * k_scale;
-  if (!(logit_scale <= 3.0e38)) return DIT_ATTN_ERR_INVALID_ARG;
+  if (!logit_scale_ok(logit_scale)) return DIT_ATTN_ERR_INVALID_ARG;
   if (d != 128) return DIT_ATTN_ERR_UNSUPPORTED;
   rc = check_workspace(workspace, workspace_bytes, q8, k8, v, out, B, H, Lq, Lk, d, 1);
   if (rc != DIT_ATTN_OK) return rc;
@@ -1082,7 +1175,7 @@ int dit_attn_forward_fp8_ws(const void* q8, const void* k8, const void* v8, void
   if (!std::isfinite(v_scale) || !(v_scale > 0.f) || !std::isfinite(1.f / v_scale))
     return DIT_ATTN_ERR_INVALID_ARG;
   const double logit_scale = static_cast<double>(scale) * q_scale * k_scale;
-  if (!(logit_scale <= 3.0e38)) return DIT_ATTN_ERR_INVALID_ARG;
+  if (!logit_scale_ok(logit_scale)) return DIT_ATTN_ERR_INVALID_ARG;
   if (d != 128) return DIT_ATTN_ERR_UNSUPPORTED;
   rc = check_workspace(workspace, workspace_bytes, q8, k8, v8, out, B, H, Lq, Lk, d, 1, 1);
   if (rc != DIT_ATTN_OK) return rc;
@@ -1107,20 +1200,33 @@ int dit_attn_forward_fp8(const void* q8, const void* k8, const void* v8, void* o
                                  v_scale, nullptr, 0, stream);
 }
 
+int dit_attn_forward_qnorm(const void* q, const void* k, const void* v, void* out, int B, int H,
+                           int Lq, int Lk, int d, float scale, const void* q_weight, float eps,
+                           void* workspace, long long workspace_bytes, void* stream) {
+  int rc = check_forward_args(q, k, v, out, B, H, Lq, Lk, d, scale, 2);
+  if (rc != DIT_ATTN_OK) return rc;
+  if (!std::isfinite(eps) || eps < 0.f) return DIT_ATTN_ERR_INVALID_ARG;
+  if (q_weight && ((reinterpret_cast<uintptr_t>(q_weight) & 15u) ||
+                   overlaps(q_weight, 2 * 128, out, static_cast<int64_t>(B) * H * Lq * d * 2)))
+    return DIT_ATTN_ERR_INVALID_ARG;
+  if (d != 128) return DIT_ATTN_ERR_UNSUPPORTED;
+  rc = check_workspace(workspace, workspace_bytes, q, k, v, out, B, H, Lq, Lk, d, 2);
+  if (rc != DIT_ATTN_OK) return rc;
+  const int64_t BH = static_cast<int64_t>(B) * H;
+  int dev = -1;
+  if (!current_device(&dev)) return DIT_ATTN_ERR_NO_DEVICE;
+  int max_pairs;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_state[dev].ready) return DIT_ATTN_ERR_NOT_INITIALIZED;
+    max_pairs = g_state[dev].max_pairs_qnorm;
+  }
+  return launch_pair<false, false, true>(q, k, v, out, BH, Lq, Lk, scale,
+                                         static_cast<cudaStream_t>(stream), max_pairs, workspace,
+                                         workspace_bytes, 1.f, q_weight, eps);
+}
+
 }  // extern "C"
-
-namespace {
-
-// Scratch of dit_attn_forward_noalloc, a file-scope device array: room for the
-// split tail's partial rows (512 x (128 + 2) fp32 per key-range chunk) of up
-// to kScratchChunks chunks.  A split plan needs at most one chunk per CTA pair
-// (74 on a B300); a larger plan runs unsplit instead.
-constexpr int64_t kScratchChunks = 80;
-constexpr int64_t kScratchBytes =
-    kScratchChunks * kPairUnitRows * (128 + 2) * static_cast<int64_t>(sizeof(float));
-static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
-
-}  // namespace
 
 extern "C" {
 
@@ -1131,8 +1237,19 @@ int dit_attn_forward_noalloc(const void* q, const void* k, const void* v, void* 
   int dev = -1;
   if (!current_device(&dev)) return DIT_ATTN_ERR_NO_DEVICE;
   void* scratch = nullptr;
-  const cudaError_t e = cudaGetSymbolAddress(&scratch, g_scratch);
-  if (e != cudaSuccess) return cuda_fail(e);
+  int max_pairs = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_state[dev].ready) return DIT_ATTN_ERR_NOT_INITIALIZED;
+    scratch = g_state[dev].scratch;
+    max_pairs = g_state[dev].max_pairs;
+  }
+  if (d == 128) {
+    const int64_t units = static_cast<int64_t>(B) * H *
+                          ((static_cast<int64_t>(Lq) + kPairUnitRows - 1) / kPairUnitRows);
+    if (plan_split(units, (Lk + dit::kBN - 1) / dit::kBN, max_pairs).ws_bytes > kScratchBytes)
+      return DIT_ATTN_ERR_UNSUPPORTED;
+  }
   return dit_attn_forward_ws(q, k, v, out, B, H, Lq, Lk, d, scale, scratch, kScratchBytes, stream);
 }
 
@@ -1140,7 +1257,7 @@ int dit_attn_workspace_size(int B, int H, int Lq, int Lk, int d, int variant, lo
   if (!bytes) return DIT_ATTN_ERR_INVALID_ARG;
   *bytes = 0;
   if (B < 1 || H < 1 || Lq < 1 || Lk < 1) return DIT_ATTN_ERR_INVALID_ARG;
-  if (variant < 0 || variant > 2) return DIT_ATTN_ERR_INVALID_ARG;
+  if (variant < 0 || variant > 3) return DIT_ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return DIT_ATTN_ERR_UNSUPPORTED;
   if (variant != 0 && d != 128) return DIT_ATTN_ERR_UNSUPPORTED;
   const int64_t BH = static_cast<int64_t>(B) * H;
@@ -1154,13 +1271,42 @@ int dit_attn_workspace_size(int B, int H, int Lq, int Lk, int d, int variant, lo
   {
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_state[dev].ready) return DIT_ATTN_ERR_NOT_INITIALIZED;
-    max_pairs = variant == 2   ? g_state[dev].max_pairs_fp8
+    max_pairs = variant == 3   ? g_state[dev].max_pairs_qnorm
+                : variant == 2 ? g_state[dev].max_pairs_fp8
                 : variant == 1 ? g_state[dev].max_pairs_qk8
                                : g_state[dev].max_pairs;
   }
   if (d == 64) return DIT_ATTN_OK;   // the d = 64 kernel never splits
   const int64_t units = BH * ((static_cast<int64_t>(Lq) + kPairUnitRows - 1) / kPairUnitRows);
   *bytes = plan_split(units, (Lk + dit::kBN - 1) / dit::kBN, max_pairs).ws_bytes;
+  return DIT_ATTN_OK;
+}
+
+int dit_attn_check_exp2(const void* x, void* y_fma, void* y_mufu, long long n, int degree,
+                        void* stream) {
+  if (!x || !y_fma || !y_mufu || n < 1 || n > (1ll << 40)) return DIT_ATTN_ERR_INVALID_ARG;
+  if (degree != 2 && degree != 3) return DIT_ATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y_fma) |
+       reinterpret_cast<uintptr_t>(y_mufu)) & 3u)
+    return DIT_ATTN_ERR_INVALID_ARG;
+  const int64_t nb = static_cast<int64_t>(n) * 4;
+  if (overlaps(x, nb, y_fma, nb) || overlaps(x, nb, y_mufu, nb) || overlaps(y_fma, nb, y_mufu, nb))
+    return DIT_ATTN_ERR_INVALID_ARG;
+  int dev = -1;
+  if (!current_device(&dev)) return DIT_ATTN_ERR_NO_DEVICE;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_state[dev].ready) return DIT_ATTN_ERR_NOT_INITIALIZED;
+  }
+  const unsigned blocks = static_cast<unsigned>((n + 255) / 256);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const float* xf = static_cast<const float*>(x);
+  float* yf = static_cast<float*>(y_fma);
+  float* ym = static_cast<float*>(y_mufu);
+  if (degree == 2) dit::exp2_check_kernel<2><<<blocks, 256, 0, s>>>(xf, yf, ym, n);
+  else dit::exp2_check_kernel<3><<<blocks, 256, 0, s>>>(xf, yf, ym, n);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
   return DIT_ATTN_OK;
 }
 
@@ -1272,18 +1418,22 @@ int dit_attn_quantize_e4m3(const void* x, void* y8, long long n, float out_scale
 int dit_attn_get_device_error(void* stream) {
   int dev = -1;
   if (!current_device(&dev)) return DIT_ATTN_ERR_NO_DEVICE;
-  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // one reader at a time: g_error_taken holds the word between the exchange
+  // kernel and the copy
+  std::lock_guard<std::mutex> lock(g_err_mu);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  dit::take_device_error_kernel<<<1, 1, 0, s>>>();
+  e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   int word = 0;
-  e = cudaMemcpyFromSymbol(&word, dit::g_device_error, sizeof(int));
+  e = cudaMemcpyFromSymbolAsync(&word, dit::g_error_taken, sizeof(int), 0,
+                                cudaMemcpyDeviceToHost, s);
   if (e != cudaSuccess) return cuda_fail(e);
-  if (word != 0) {
-    const int zero = 0;
-    e = cudaMemcpyToSymbol(dit::g_device_error, &zero, sizeof(int));
-    if (e != cudaSuccess) return cuda_fail(e);
-    return word;
-  }
-  return DIT_ATTN_OK;
+  e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return word != 0 ? word : DIT_ATTN_OK;
 }
 
 }  // extern "C"

@@ -91,15 +91,19 @@ struct PairTraitsT {
   static constexpr int kBarPFull = kBarSFull + 2;    // leader: 16 warp arrivals
   static constexpr int kBarOFull = kBarPFull + 2;    // both
   static constexpr int kBarDrain = kBarOFull + 2;    // leader
-  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kBarProdDone = kBarDrain + 1; // leader: both producers reported
+  static constexpr int kBarQReady = kBarProdDone + 1;// leader: both CTAs' tile t normalised (2)
+  static constexpr int kNumBars = kBarQReady + 2;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr uint32_t kSmemBytes = 1024 + kOffMisc + 16;
+  static constexpr uint32_t kSmemBytes = 1024 + kOffMisc + kMiscWords * 4;
   static constexpr uint32_t kPFullArrivals = 16;     // 8 softmax warps x 2 CTAs
 };
 using PairTraits = PairTraitsT<false>;
 
 // ----------------------------------------------------------------- producer (both CTAs)
-template <bool kQK8, bool kPV8>
+// With kNormQ each CTA's query tile completes on the CTA's own barrier (its
+// own normalisation warps wait for it); otherwise on the leader's.
+template <bool kQK8, bool kPV8, bool kNormQ>
 __device__ void pair_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                const CUtensorMap* tmV, const Params& p, const Shared& sh) {
   using T = PairTraitsT<kQK8, kPV8>;
@@ -109,19 +113,29 @@ __device__ void pair_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
   const uint64_t pol_q = policy_evict_first();
   const uint32_t full0_leader = mapa_shared(sh.bar(T::kBarFull), 0);
   const uint32_t qfull0_leader = mapa_shared(sh.bar(T::kBarQFull), 0);
-  uint32_t stage = 0, phase = 0, n_fills = 0, q_fills = 0, q_parity = 0, it = 0;
+  // fills: K/V half-stage copies issued so far (stage = fills mod kStages);
+  // q_loads0/1: query-tile-0/1 copies issued so far.  Both are left in shared
+  // memory for the teardown drain.
+  uint32_t stage = 0, phase = 0, fills = 0, it = 0, q_loads0 = 0, q_loads1 = 0;
   bool ok = true;
   const int n_kv = (p.Lk + kBN - 1) / kBN;
 
   auto load_q = [&](int t, int bh, int row0) -> bool {
     if (!mbar_wait(sh.bar(T::kBarQEmpty + t), (it & 1u) ^ 1u, kWaitLimitNs, sh.abort)) return false;
-    if (leader) mbar_arrive_expect_tx(sh.bar(T::kBarQFull + t), 2 * T::kQTileBytes);
     const uint32_t dst = sh.base + T::kOffQ + t * T::kQTileBytes;
-    for (int b = 0; b < T::kQKBoxes; ++b)
-      tma_load_3d_pair(dst + b * T::kQBoxBytes, tmQ, qfull0_leader + 8u * t, b * T::kBoxCols,
-                       row0 + t * kBM, bh, pol_q);
-    q_fills |= 1u << t;
-    q_parity = (q_parity & ~(1u << t)) | ((it & 1u) << t);
+    if constexpr (kNormQ) {
+      mbar_arrive_expect_tx(sh.bar(T::kBarQFull + t), T::kQTileBytes);
+      for (int b = 0; b < T::kQKBoxes; ++b)
+        tma_load_3d(dst + b * T::kQBoxBytes, tmQ, sh.bar(T::kBarQFull + t), b * T::kBoxCols,
+                    row0 + t * kBM, bh, pol_q);
+    } else {
+      if (leader) mbar_arrive_expect_tx(sh.bar(T::kBarQFull + t), 2 * T::kQTileBytes);
+      for (int b = 0; b < T::kQKBoxes; ++b)
+        tma_load_3d_pair(dst + b * T::kQBoxBytes, tmQ, qfull0_leader + 8u * t, b * T::kBoxCols,
+                         row0 + t * kBM, bh, pol_q);
+    }
+    if (t == 0) ++q_loads0;
+    else ++q_loads1;
     return true;
   };
   auto take_empty = [&](uint32_t half_bytes) -> bool {
@@ -130,7 +144,7 @@ __device__ void pair_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
     return true;
   };
   auto advance = [&]() {
-    if (n_fills < T::kStages) ++n_fills;
+    ++fills;
     if (++stage == T::kStages) { stage = 0; phase ^= 1u; }
   };
 
@@ -163,27 +177,63 @@ __device__ void pair_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
       advance();
     }
   }
-  if (!ok) {
-    record_timeout<true>(sh);
-    // Let this CTA's copies in flight land before its shared memory goes away.
-    // Their completion is counted on the leader's barriers, so the leader waits.
-    if (leader) {
-      const volatile int no_abort = 0;
-      uint32_t s = stage, ph = phase;
-      for (uint32_t f = 0; f < n_fills; ++f) {
-        if (s == 0) { s = T::kStages - 1; ph ^= 1u; } else { --s; }
-        mbar_wait(sh.bar(T::kBarFull + s), ph, kWaitLimitNs, &no_abort);
-      }
-      for (int t = 0; t < 2; ++t)
-        if (q_fills & (1u << t))
-          mbar_wait(sh.bar(T::kBarQFull + t), (q_parity >> t) & 1u, kWaitLimitNs, &no_abort);
-    } else {
-      // The peer cannot wait on the leader's barriers; a TMA copy lands within
-      // microseconds, so give the last ones 200 us.
-      const uint64_t t0 = globaltimer_ns();
-      while (globaltimer_ns() - t0 < 200000ull) {
-      }
-    }
+  if (!ok) record_timeout<true>(sh);
+  // Report the copies issued to the leader (for the teardown drain).
+  if (leader) {
+    st_shared_u32(sh.misc_word(kMiscFills), fills);
+    st_shared_u32(sh.misc_word(kMiscQLoads), q_loads0);
+    st_shared_u32(sh.misc_word(kMiscQLoads + 1), q_loads1);
+    mbar_arrive(sh.bar(T::kBarProdDone));
+  } else {
+    st_shared_cluster_u32(mapa_shared(sh.misc_word(kMiscPeerFills), 0), fills);
+    st_shared_cluster_u32(mapa_shared(sh.misc_word(kMiscPeerQLoads), 0), q_loads0);
+    st_shared_cluster_u32(mapa_shared(sh.misc_word(kMiscPeerQLoads + 1), 0), q_loads1);
+    mbar_arrive_release_cluster(mapa_shared(sh.bar(T::kBarProdDone), 0));
+  }
+}
+
+// Teardown after a bounded wait gave up (one thread of the leader CTA, once
+// its own role has returned): every copy either CTA issued must land before
+// the CTAs' shared memory goes away.  Both producers report how many copies
+// they issued and arrive on the leader's producer-done barrier.  All copies
+// complete on the leader's barriers, and a barrier phase only completes when
+// the leader armed it for both halves and both halves landed, but the two
+// producers may have stopped at different points.  For each of the last
+// kStages K/V fills and each query tile's last load, the leader balances the
+// phase: where only the leader issued the fill it retires the missing half's
+// bytes itself (mbarrier.complete_tx), where only the peer did it arms the
+// phase for that half alone; then it waits (bounded) for the phase.
+template <class T, bool kNormQ>
+__device__ void pair_teardown_drain(const Shared& sh) {
+  const volatile int no_abort = 0;
+  if (!mbar_wait_acquire_cluster(sh.bar(T::kBarProdDone), 0, kWaitLimitNs)) return;
+  auto word = [&](int i) { return ld_shared_u32(sh.misc_word(i)); };
+  auto balance_and_wait = [&](uint32_t bar, bool by_leader, bool by_peer, uint32_t half_bytes,
+                              uint32_t parity) {
+    if (by_leader && !by_peer) mbar_complete_tx(bar, half_bytes);
+    if (by_peer && !by_leader) mbar_arrive_expect_tx(bar, half_bytes);
+    mbar_wait(bar, parity, kWaitLimitNs, &no_abort);
+  };
+  // fill counts of the two producers differ by at most kStages (each waits
+  // for the consumption of the fill kStages back, which needs both halves)
+  const uint32_t fl = word(kMiscFills), fp = word(kMiscPeerFills);
+  const uint32_t last = static_cast<int32_t>(fp - fl) > 0 ? fp : fl;
+  const uint32_t window = last < static_cast<uint32_t>(T::kStages) ? last : T::kStages;
+  for (uint32_t k = 1; k <= window; ++k) {
+    const uint32_t f = last - k;   // fills alternate K half (even f), V half (odd f)
+    balance_and_wait(sh.bar(T::kBarFull + static_cast<int>(f % T::kStages)),
+                     static_cast<int32_t>(f - fl) < 0, static_cast<int32_t>(f - fp) < 0,
+                     (f & 1u) ? T::kVHalfBytes : T::kKHalfBytes, (f / T::kStages) & 1u);
+  }
+  // query tiles: the two producers' load counts differ by at most one (with
+  // kNormQ each CTA's tiles complete locally and its normalisation warps
+  // drain them)
+  for (int t = 0; t < 2 && !kNormQ; ++t) {
+    const uint32_t ql = word(kMiscQLoads + t), qp = word(kMiscPeerQLoads + t);
+    const uint32_t q_last = static_cast<int32_t>(qp - ql) > 0 ? qp : ql;
+    if (q_last == 0) continue;
+    balance_and_wait(sh.bar(T::kBarQFull + t), ql == q_last, qp == q_last, T::kQTileBytes,
+                     (q_last - 1u) & 1u);
   }
 }
 
@@ -232,7 +282,7 @@ __device__ __forceinline__ void pair_issue_pv(uint32_t d_tmem, uint32_t p_tmem, 
   }
 }
 
-template <bool kQK8, bool kPV8>
+template <bool kQK8, bool kPV8, bool kNormQ>
 __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) {
   using T = PairTraitsT<kQK8, kPV8>;
   constexpr uint16_t kBoth = 3;
@@ -254,6 +304,15 @@ __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) 
     if (++stage == T::kStages) { stage = 0; phase ^= 1u; }
     return true;
   };
+  // query tile t of this item in both CTAs' shared memory (normalised, with
+  // kNormQ: written by other threads, hence the cluster-scope acquire)
+  auto wait_q = [&](int t) -> bool {
+    if constexpr (kNormQ)
+      return __all_sync(0xffffffffu, mbar_wait_acquire_cluster(sh.bar(T::kBarQReady + t), it & 1u,
+                                                               kWaitLimitNs, sh.abort));
+    else
+      return wait(T::kBarQFull + t, it & 1u);
+  };
 
   // Stage waits for the next key tile (its V and the following K) happen while
   // the warp waits for P_1 anyway, off the path from P-ready to the next MMA.
@@ -267,7 +326,7 @@ __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) 
       n = (s + 1) * n_kv / p.splits - s * n_kv / p.splits;
     }
     uint32_t sK = 0, sV = 0, sK_next = 0, sV_next = 0;
-    ok = wait(T::kBarQFull + 0, it & 1u) && take_stage(sK);
+    ok = wait_q(0) && take_stage(sK);
     if (!ok) break;
     tc_fence_after();
     if (issuer) {
@@ -276,7 +335,7 @@ __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) 
       if (n == 1) mma_commit_pair(sh.bar(T::kBarQEmpty + 0), kBoth);
     }
     __syncwarp();
-    ok = wait(T::kBarQFull + 1, it & 1u) && take_stage(sV) && (n == 1 || take_stage(sK_next));
+    ok = wait_q(1) && take_stage(sV) && (n == 1 || take_stage(sK_next));
     if (!ok) break;
     tc_fence_after();
     if (issuer) {
@@ -336,19 +395,40 @@ __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) 
 }
 
 // ----------------------------------------------------------------- softmax (pair kernel)
+// Largest scaled logit s * scale_log2 of 32 logits, keys at or beyond `valid`
+// excluded (-inf when all are).  Scaling is monotone, so this is scale_log2
+// times the largest raw logit when scale_log2 >= 0 and times the smallest
+// when it is negative; the sign is the same for the whole launch.
 template <bool kMasked>
-__device__ __forceinline__ float rowmax_chunk(const uint32_t (&sr)[32], int key0, int valid) {
-  float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+__device__ __forceinline__ float rowmax_chunk(const uint32_t (&sr)[32], int key0, int valid,
+                                              float scale_log2) {
+  const bool neg = scale_log2 < 0.f;
+  const float sentinel = neg ? INFINITY : -INFINITY;
+  float m[4] = {sentinel, sentinel, sentinel, sentinel};
+  if (!neg) {
 #pragma unroll
-  for (int i = 0; i < 32; i += 2) {
-    float a = __uint_as_float(sr[i]), b = __uint_as_float(sr[i + 1]);
-    if (kMasked) {
-      a = (key0 + i < valid) ? a : -INFINITY;
-      b = (key0 + i + 1 < valid) ? b : -INFINITY;
+    for (int i = 0; i < 32; i += 2) {
+      float a = __uint_as_float(sr[i]), b = __uint_as_float(sr[i + 1]);
+      if (kMasked) {
+        a = (key0 + i < valid) ? a : -INFINITY;
+        b = (key0 + i + 1 < valid) ? b : -INFINITY;
+      }
+      m[(i / 2) & 3] = fmax3(m[(i / 2) & 3], a, b);
     }
-    m[(i / 2) & 3] = fmax3(m[(i / 2) & 3], a, b);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      float a = __uint_as_float(sr[i]), b = __uint_as_float(sr[i + 1]);
+      if (kMasked) {
+        a = (key0 + i < valid) ? a : INFINITY;
+        b = (key0 + i + 1 < valid) ? b : INFINITY;
+      }
+      m[(i / 2) & 3] = fmin3(m[(i / 2) & 3], a, b);
+    }
   }
-  return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+  const float e = neg ? fminf(fminf(m[0], m[1]), fminf(m[2], m[3]))
+                      : fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+  return e == sentinel ? -INFINITY : e * scale_log2;
 }
 
 // Probabilities of 32 logits rounded to e4m3, four keys per word (key order =
@@ -365,8 +445,19 @@ __device__ __forceinline__ void probs_chunk_e4m3(const uint32_t (&sr)[32], float
         __ffma2_rn(make_float2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), sl2, nm);
     const float2 x23 =
         __ffma2_rn(make_float2(__uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3])), sl2, nm);
-    float p0 = ex2_approx(x01.x), p1 = ex2_approx(x01.y);
-    float p2 = ex2_approx(x23.x), p3 = ex2_approx(x23.y);
+    float p0, p1, p2, p3;
+    if ((kExp2FmaQuadsE4M3 >> (i / 4)) & 1u) {   // this quad's exp2 on the FMA pipe
+      const float2 e01 = exp2_fma_pair<2>(x01), e23 = exp2_fma_pair<2>(x23);
+      p0 = e01.x;
+      p1 = e01.y;
+      p2 = e23.x;
+      p3 = e23.y;
+    } else {
+      p0 = ex2_approx(x01.x);
+      p1 = ex2_approx(x01.y);
+      p2 = ex2_approx(x23.x);
+      p3 = ex2_approx(x23.y);
+    }
     if (kMasked) {
       p0 = (key0 + i < valid) ? p0 : 0.f;
       p1 = (key0 + i + 1 < valid) ? p1 : 0.f;
@@ -410,9 +501,9 @@ __device__ __forceinline__ void softmax_tile_lean(uint32_t taddr_s, int key0, bo
       else probs_chunk<false>(sr, scale_log2, -m, key0 + 32 * c, kBN, &pk[16 * c], acc);
     }
   };
-  auto chunk_max = [&](int c) -> float {
-    return masked ? rowmax_chunk<true>(sr, key0 + 32 * c, valid)
-                  : rowmax_chunk<false>(sr, key0 + 32 * c, kBN);
+  auto chunk_max = [&](int c) -> float {   // largest scaled logit of chunk c
+    return masked ? rowmax_chunk<true>(sr, key0 + 32 * c, valid, scale_log2)
+                  : rowmax_chunk<false>(sr, key0 + 32 * c, kBN, scale_log2);
   };
   auto clear = [&]() {
 #pragma unroll
@@ -425,8 +516,7 @@ __device__ __forceinline__ void softmax_tile_lean(uint32_t taddr_s, int key0, bo
     float mx = chunk_max(0);
     load(1);
     mx = fmaxf(mx, chunk_max(1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-    const float m_tile = mx * scale_log2;
+    const float m_tile = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
     float factor = 1.f;
     if (m_tile > m_used + kThreshold) {
       factor = ex2_approx(m_used - m_tile);   // 0 on the first tile
@@ -551,23 +641,108 @@ __device__ void softmax_role_pair(const Params& p, const Shared& sh, uint32_t tm
   if (!ok) record_timeout<true>(sh);
 }
 
+// ----------------------------------------------------------------- query normalisation (kNormQ)
+// Warps 18-19 of each CTA (64 threads): as each of this CTA's query tiles
+// lands, RMS-normalise its 128 rows in place in shared memory with exactly
+// the arithmetic of dit_attn_rmsnorm (16 lanes per row, 8 columns a lane,
+// fp32 sum of squares in the same order, xor-shuffle reduction, rsqrt, times
+// the weight, rounded to nearest-even bf16), make the writes visible to the
+// tensor cores (async proxy) and report the tile ready on the leader's
+// barrier with a cluster-scope release.  A query tile lands one or two key
+// tiles before the MMA warp needs it, so the pass stays off the MMA chain.
+template <class T>
+__device__ void pair_qnorm_role(const Params& p, const Shared& sh) {
+  const int tid = static_cast<int>(threadIdx.x) - 18 * 32;     // 0..63
+  const int lane = threadIdx.x & 31;
+  const int chunk = lane & 15;                                  // columns 8*chunk .. +7
+  const int row_in = (tid >> 5) * 2 + (lane >> 4);             // row within a step of 4
+  const uint32_t ready_leader = mapa_shared(sh.bar(T::kBarQReady), 0);
+  float wf[8];
+  if (p.q_weight) {
+    const uint4 wv = reinterpret_cast<const uint4*>(p.q_weight)[chunk];
+    const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      wf[2 * i] = __uint_as_float(ww[i] << 16);
+      wf[2 * i + 1] = __uint_as_float(ww[i] & 0xFFFF0000u);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) wf[i] = 1.f;
+  }
+  const float eps = p.q_eps;
+  uint32_t it = 0;
+  int stuck_tile = -1;   // the tile whose landing a give-up left unobserved
+  for (int i = static_cast<int>(cluster_id_x()); i < p.num_items && stuck_tile < 0;
+       i += static_cast<int>(num_clusters_x()), ++it) {
+    for (int t = 0; t < 2; ++t) {
+      const bool got = mbar_wait(sh.bar(T::kBarQFull + t), it & 1u, kWaitLimitNs, sh.abort);
+      if (!__all_sync(0xffffffffu, got)) { stuck_tile = t; break; }
+      const uint32_t tile = sh.base + T::kOffQ + t * T::kQTileBytes;
+#pragma unroll 1
+      for (int r0 = 0; r0 < kBM; r0 += 4) {
+        const int r = r0 + row_in;
+        // 128-byte swizzle: 16-byte unit c of a 128-byte row r sits at unit c ^ (r mod 8)
+        const uint32_t addr = tile + (chunk >> 3) * T::kQBoxBytes + r * 128 +
+                              ((((chunk & 7) ^ (r & 7))) << 4);
+        const uint4 v = ld_shared_v4(addr);
+        const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+        float f[8];
+        float ss = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          f[2 * k] = __uint_as_float(vv[k] << 16);
+          f[2 * k + 1] = __uint_as_float(vv[k] & 0xFFFF0000u);
+          ss = fmaf(f[2 * k], f[2 * k], ss);
+          ss = fmaf(f[2 * k + 1], f[2 * k + 1], ss);
+        }
+#pragma unroll
+        for (int off = 8; off > 0; off /= 2) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        const float inv = rsqrtf(ss * (1.f / T::D) + eps);
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          o[k] = pack_bf16x2(f[2 * k] * inv * wf[2 * k], f[2 * k + 1] * inv * wf[2 * k + 1]);
+        st_shared_v4(addr, make_uint4(o[0], o[1], o[2], o[3]));
+      }
+      fence_proxy_async_shared();
+      named_bar_sync(1, 64);
+      if (tid == 0) mbar_arrive_release_cluster(ready_leader + 8u * static_cast<uint32_t>(t));
+    }
+  }
+  if (stuck_tile >= 0) {
+    if (tid == 0) {
+      record_timeout<true>(sh);
+      // copies of this item's query tiles may still be in flight: let them land
+      const volatile int no_abort = 0;
+      for (int t = stuck_tile; t < 2; ++t)
+        mbar_wait(sh.bar(T::kBarQFull + t), it & 1u, kWaitLimitNs, &no_abort);
+    }
+    __syncwarp();
+  }
+}
+
 // ----------------------------------------------------------------- kernel
 // Launched with a cluster dimension of 2 (consecutive CTAs form a pair).
-template <bool kQK8, bool kPV8>
+// kNormQ (bf16 only): queries arrive un-normalised and warps 18-19
+// RMS-normalise each tile in shared memory before its first product.
+template <bool kQK8, bool kPV8, bool kNormQ = false>
 __global__ void __launch_bounds__(kPairThreads, 1)
     fmha_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const Params p) {
   using T = PairTraitsT<kQK8, kPV8>;
+  static_assert(!(kNormQ && kQK8), "the fused query normalisation is a bf16-query variant");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
-  uint32_t* misc = reinterpret_cast<uint32_t*>(base_ptr + T::kOffMisc);  // [0] TMEM, [1] abort
+  uint32_t* misc = reinterpret_cast<uint32_t*>(base_ptr + T::kOffMisc);
   Shared sh;
   sh.base = base;
   sh.bar0 = base + T::kOffBar;
-  sh.abort = reinterpret_cast<volatile int*>(misc + 1);
+  sh.abort = reinterpret_cast<volatile int*>(misc + kMiscAbort);
+  sh.misc = base + T::kOffMisc;
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   const bool leader = cluster_ctarank() == 0;
@@ -585,6 +760,8 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       mbar_init(sh.bar(T::kBarOFull + t), 1);
     }
     mbar_init(sh.bar(T::kBarDrain), 1);
+    mbar_init(sh.bar(T::kBarProdDone), 2);
+    for (int t = 0; t < 2; ++t) mbar_init(sh.bar(T::kBarQReady + t), 2);
     *sh.abort = 0;
     fence_mbarrier_init();
   }
@@ -594,7 +771,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     tma_prefetch_desc(&tmV);
   }
   if (warp == kPairMmaWarp) {
-    tmem_alloc_pair(smem_u32(misc), T::kTmemCols);
+    tmem_alloc_pair(smem_u32(misc + kMiscTmem), T::kTmemCols);
     tmem_relinquish_pair();
   }
   // Both CTAs' barriers and TMEM exist before either CTA touches the other's.
@@ -602,24 +779,27 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   __syncthreads();
   cluster_sync_all();
   tc_fence_after();
-  const uint32_t tmem = misc[0];
+  const uint32_t tmem = misc[kMiscTmem];
 
   if (warp < kPairMmaWarp) {
     reg_alloc<kPairRegsSoftmax>();
     softmax_role_pair<T::D, T>(p, sh, tmem);
+    if (leader && threadIdx.x == 0 && *sh.abort) pair_teardown_drain<T, kNormQ>(sh);
   } else if (warp == kPairMmaWarp) {
     reg_dealloc<kPairRegsOther>();
-    if (leader) pair_mma_role<kQK8, kPV8>(p, sh, tmem);
+    if (leader) pair_mma_role<kQK8, kPV8, kNormQ>(p, sh, tmem);
   } else if (warp == kPairLoadWarp) {
     reg_dealloc<kPairRegsOther>();
-    if (lane == 0) pair_load_role<kQK8, kPV8>(&tmQ, &tmK, &tmV, p, sh);
+    if (lane == 0) pair_load_role<kQK8, kPV8, kNormQ>(&tmQ, &tmK, &tmV, p, sh);
     __syncwarp();
   } else {
     reg_dealloc<kPairRegsOther>();
+    if constexpr (kNormQ) pair_qnorm_role<T>(p, sh);
   }
 
-  // The leader drained its MMAs; neither CTA leaves while the pair's MMAs or
-  // copies could still touch its shared memory or TMEM.
+  // The leader drained its MMAs and, after a give-up, every copy either CTA
+  // issued; neither CTA leaves while the pair's MMAs or copies could still
+  // touch its shared memory or TMEM.
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();

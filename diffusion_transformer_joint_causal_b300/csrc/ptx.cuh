@@ -248,8 +248,77 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
+// Arrive with release semantics at cluster scope: this thread's earlier
+// writes to the cluster's shared memory are visible to a thread that
+// observes the phase with mbar_wait_acquire_cluster.
+__device__ __forceinline__ void mbar_arrive_release_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+// Bounded wait for a phase of a local barrier with acquire semantics at
+// cluster scope (pairs with mbar_arrive_release_cluster); gives up after
+// limit_ns or once *abort is set (if given).
+__device__ __forceinline__ bool mbar_wait_acquire_cluster(uint32_t bar, uint32_t parity,
+                                                          uint64_t limit_ns,
+                                                          const volatile int* abort = nullptr) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (abort && *abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+// Make this thread's generic-proxy writes to shared memory visible to later
+// async-proxy reads (tensor-core operands, TMA).
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Named barrier `id` over `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
 __device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_shared_cluster_u32(uint32_t cluster_addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
+// Retire `bytes` of an mbarrier's pending transaction count without a copy
+// (as if that many bytes had landed); no arrival.
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
 }
 // TMEM allocation for pair MMAs: one warp of each CTA of the pair runs these.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
@@ -387,6 +456,12 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // lo_acc += bf16 in bits [15:0] of w, hi_acc += bf16 in bits [31:16] of w
 // (mixed-precision f32 += bf16 adds, exact widening of the bf16 operand).
 __device__ __forceinline__ void add_bf16x2_halves(float& lo_acc, float& hi_acc, uint32_t w) {
@@ -396,6 +471,64 @@ __device__ __forceinline__ void add_bf16x2_halves(float& lo_acc, float& hi_acc, 
       "add.rn.f32.bf16 %1, hi, %1;\n\t}"
       : "+f"(lo_acc), "+f"(hi_acc)
       : "r"(w));
+}
+
+// ----------------------------------------------------------------- exp2 on the FMA pipe
+// 2^x for a pair of arguments without the MUFU unit, so that the softmax can
+// move part of its exponentials off the multi-function pipe.  Cody-Waite
+// range reduction (Cody and Waite, "Software Manual for the Elementary
+// Functions", 1980): 2^x = 2^j * p(f) with j = rint(x), f = x - j in
+// [-1/2, 1/2] and p the minimax polynomial (relative error) of degree 2 or 3
+// for 2^f on that interval, from the Remez exchange (exp2_poly.py derives the
+// coefficients: largest relative error 1.73e-3 for degree 2, 7.5e-5 for
+// degree 3, Horner in fp32).
+//
+// The argument is first clamped and mapped by one saturating FMA, y =
+// sat(x / 252 + 125 / 252), so that y in [0, 1] stands for x clamped to
+// [-125, 127]; the rounding of y and of the two constants moves x by at most
+// 1.9e-5, a relative 1.3e-5 in the result, on top of the polynomial's error.
+// With M = 1.5 * 2^23, t = 252 y + (M - 125)
+// rounds x to the integer j (t = M + j exactly), -125 - j = (M - 125) - t and
+// f = 252 y + (-125 - j) are exact, and p(f) * 2^j is p's bit pattern plus
+// j << 23 (t's bit pattern shifted left by 23 is j << 23 modulo 2^32, since
+// M's low 9 bits are zero).  The clamp keeps every result a normal float,
+// 2^-125.5 <= result <= 2^127.5, where 2^x itself would underflow or overflow.
+constexpr float kExp2D2C0 = 1.0004431009292603f, kExp2D2C1 = 0.7034479975700378f,
+                kExp2D2C2 = 0.23842893540859222f;
+constexpr float kExp2D3C0 = 0.9999280571937561f, kExp2D3C1 = 0.6932609677314758f,
+                kExp2D3C2 = 0.2426111251115799f, kExp2D3C3 = 0.0551716685295105f;
+
+__device__ __forceinline__ float fma_sat(float a, float b, float c) {
+  float d;
+  asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+template <int kDeg>
+__device__ __forceinline__ float2 exp2_fma_pair(float2 x) {
+  static_assert(kDeg == 2 || kDeg == 3, "polynomial degree");
+  constexpr float kM = 12582912.0f;   // 1.5 * 2^23
+  const float2 y = make_float2(fma_sat(x.x, 1.f / 252.f, 125.f / 252.f),
+                               fma_sat(x.y, 1.f / 252.f, 125.f / 252.f));
+  const float2 k252 = make_float2(252.f, 252.f);
+  const float2 m125 = make_float2(kM - 125.f, kM - 125.f);
+  const float2 t = __ffma2_rn(y, k252, m125);
+  const float2 nj = __ffma2_rn(t, make_float2(-1.f, -1.f), m125);   // -125 - j
+  const float2 f = __ffma2_rn(y, k252, nj);
+  float2 p;
+  if constexpr (kDeg == 3) {
+    p = __ffma2_rn(f, make_float2(kExp2D3C3, kExp2D3C3),
+                   make_float2(kExp2D3C2, kExp2D3C2));
+    p = __ffma2_rn(p, f, make_float2(kExp2D3C1, kExp2D3C1));
+    p = __ffma2_rn(p, f, make_float2(kExp2D3C0, kExp2D3C0));
+  } else {
+    p = __ffma2_rn(f, make_float2(kExp2D2C2, kExp2D2C2),
+                   make_float2(kExp2D2C1, kExp2D2C1));
+    p = __ffma2_rn(p, f, make_float2(kExp2D2C0, kExp2D2C0));
+  }
+  return make_float2(
+      __int_as_float(__float_as_int(p.x) + static_cast<int>(__float_as_uint(t.x) << 23)),
+      __int_as_float(__float_as_int(p.y) + static_cast<int>(__float_as_uint(t.y) << 23)));
 }
 
 // Four fp32 -> four e4m3 bytes (round to nearest even, saturating at +-448),

@@ -44,7 +44,7 @@ extern "C" {
 
 typedef enum dit_attn_status {
   DIT_ATTN_OK = 0,
-  DIT_ATTN_ERR_INVALID_ARG = 1,     /* null / misaligned pointer, size < 1, bad scale, overlap */
+  DIT_ATTN_ERR_INVALID_ARG = 1,     /* null / misaligned pointer, size < 1, unusable scale, overlap */
   DIT_ATTN_ERR_UNSUPPORTED = 2,     /* head dim other than 64 or 128; sizes beyond the limits */
   DIT_ATTN_ERR_NOT_INITIALIZED = 3, /* dit_attn_create() not called for the current device */
   DIT_ATTN_ERR_NO_DEVICE = 4,       /* no CUDA device, or the current device is not sm_103 */
@@ -69,7 +69,11 @@ int dit_attn_create(void);
  *   B, H, Lq, Lk >= 1; B*H < 2^31; Lq, Lk <= 2^31 - 513;
  *   B*H*ceil(Lq/256) < 2^31 (else UNSUPPORTED).
  *   d in {64, 128}.
- *   scale finite and >= 0 (1/sqrt(d) for a standard transformer).
+ *   scale finite, of either sign (1/sqrt(d) for a standard transformer), with
+ *   |scale| * log2(e) within fp32 range, i.e. |scale| <= 2.35e38 (else
+ *   INVALID_ARG).  The kernels form scale * log2(e) * (q . k) in fp32; logits
+ *   beyond fp32 range (only possible with extreme scales or inputs) give
+ *   unspecified outputs.
  * Asynchronous: returns after the launch.  A launch failure returns
  * DIT_ATTN_ERR_CUDA; a device-side wait that gave up is reported later by
  * dit_attn_get_device_error.
@@ -97,20 +101,35 @@ int dit_attn_forward_ws(const void* q, const void* k, const void* v, void* out, 
                         long long workspace_bytes, void* stream);
 
 /*
- * dit_attn_forward with the split tail's workspace taken from a scratch array
- * that the library holds in device memory for its whole lifetime (about 21 MB,
- * reserved when the library loads): the call itself allocates nothing and
- * needs no workspace argument.  The scratch is shared by every call on a
- * device, so calls through this entry point must not overlap in time (one
- * stream, or ordered streams); a split plan larger than the scratch runs
- * unsplit.  Arguments, results and errors as dit_attn_forward_ws.
+ * dit_attn_forward for callers that cannot allocate device memory while they
+ * run: an inference engine that reserves all device memory up front and
+ * forbids later allocations, code running inside a memory allocator's own
+ * callback, or a latency-bound loop that must not enter cudaMalloc (which can
+ * synchronise the device).  The pages have no counterpart of this entry
+ * point; it exists for embedding.  The split tail's scratch is a file-scope device array of
+ * the library, 80 key-range chunks of 512 x 130 fp32 (21.3 MB), resident on
+ * every device from when the library's device code is loaded there (at the
+ * latest, its first kernel launch or dit_attn_create) until the process exits.
+ * dit_attn_create() takes the array's device address for the current device;
+ * the call itself allocates nothing (no cudaMalloc, no library allocator) and
+ * takes no workspace argument.
+ *   Every call on a device shares the one array and leaves its contents
+ *   behind; each call writes every scratch word it later reads, so nothing
+ *   needs clearing.  Calls through this entry point that overlap on the GPU
+ *   (unordered streams) race on the scratch and give wrong results: keep
+ *   them on one stream, or order the streams.
+ *   A split plan needs at most one chunk per CTA pair (74 on a 148-SM B300);
+ *   a plan beyond the 80 chunks returns UNSUPPORTED.
+ *   Before dit_attn_create() on the current device: NOT_INITIALIZED.
+ * Arguments, results and other errors as dit_attn_forward_ws.
  */
 int dit_attn_forward_noalloc(const void* q, const void* k, const void* v, void* out, int B, int H,
                              int Lq, int Lk, int d, float scale, void* stream);
 
 /*
  * Workspace bytes that dit_attn_forward_ws (variant 0), dit_attn_forward_qk8_ws
- * (variant 1) or dit_attn_forward_fp8_ws (variant 2) uses for these sizes on
+ * (variant 1), dit_attn_forward_fp8_ws (variant 2) or dit_attn_forward_qnorm
+ * (variant 3) uses for these sizes on
  * the current device; 0 when no split applies (d = 64, or the last wave is
  * full or its units too short).  Another variant is INVALID_ARG.  Size
  * arguments as for the forward calls; requires dit_attn_create().
@@ -133,8 +152,9 @@ int dit_attn_workspace_size(int B, int H, int Lq, int Lk, int d, int variant, lo
  * k8 : the same for keys, [B, H, Lk, d], with k_scale
  * v, out: bf16, as in dit_attn_forward.
  * d must be 128 (else UNSUPPORTED).  q_scale, k_scale finite and >= 0, and
- * scale*q_scale*k_scale at most 3e38 (else INVALID_ARG); the product is
- * folded into the softmax scale once.  Arithmetic: e4m3 tensor-core products
+ * the logit scale scale*q_scale*k_scale (either sign) within the bound that
+ * dit_attn_forward sets for scale (else INVALID_ARG); the product is folded
+ * into the softmax scale once.  Arithmetic: e4m3 tensor-core products
  * with exact fp32 accumulation for S; the softmax, P (bf16), P.V and the
  * output as in dit_attn_forward.  Sizes, alignment, overlap, stream and error
  * behaviour as in dit_attn_forward (q8, k8 sizes counted in bytes).
@@ -164,8 +184,9 @@ int dit_attn_forward_qk8_ws(const void* q8, const void* k8, const void* v, void*
  * q8, k8 as in dit_attn_forward_qk8; v8: device pointer, e4m3 codes,
  * contiguous [B, H, Lk, d], dequantised value = code value * v_scale.  out:
  * bf16 [B, H, Lq, d].  d must be 128 (else UNSUPPORTED).  q_scale, k_scale
- * finite and >= 0, v_scale finite and > 0 with a finite reciprocal, and
- * scale*q_scale*k_scale at most 3e38 (else INVALID_ARG).  Arithmetic: both
+ * finite and >= 0, v_scale finite and > 0 with a finite reciprocal, and the
+ * logit scale scale*q_scale*k_scale as in dit_attn_forward_qk8 (else
+ * INVALID_ARG).  Arithmetic: both
  * products on e4m3 tensor cores with exact fp32 accumulation; every p is
  * rounded to e4m3 for P.V (relative error at most 2^-4 where p >= 2^-6, i.e.
  * for every key within 2^-9 of the row's largest weight) while the row sum
@@ -182,6 +203,32 @@ int dit_attn_forward_fp8_ws(const void* q8, const void* k8, const void* v8, void
                             int H, int Lq, int Lk, int d, float scale, float q_scale,
                             float k_scale, float v_scale, void* workspace,
                             long long workspace_bytes, void* stream);
+
+/*
+ * dit_attn_forward_ws with the queries' RMS normalisation done inside the
+ * attention kernel (the 1024x1024 and 2048x2048 workloads normalise Q and K
+ * per token and head before attention; the pages do not print it):
+ *
+ *     qn[b,h,i,:] = bf16( q[b,h,i,:] / sqrt(mean_c q[b,h,i,c]^2 + eps) * q_weight[:] )
+ *     out = softmax(qn k^T * scale) v
+ *
+ * with exactly dit_attn_rmsnorm's arithmetic, so the result equals
+ * dit_attn_rmsnorm followed by dit_attn_forward_ws (same workspace) bit for
+ * bit.  Each query tile is normalised in shared memory once, after its load
+ * and before its first product, by warps of the kernel that otherwise idle;
+ * it saves the separate pass over Q (read + write of the query tensor).  Keys
+ * are re-read for every query block, so they stay on the dit_attn_rmsnorm
+ * prologue.
+ *   q: device bf16 [B, H, Lq, d], un-normalised; k: normalised as the caller
+ *   wants; v, out, workspace as in dit_attn_forward_ws.
+ *   q_weight: NULL (all ones) or device bf16 [d], 16-byte aligned, not
+ *   overlapping out.  eps finite and >= 0 (else INVALID_ARG).  d must be 128
+ *   (else UNSUPPORTED).  Workspace sizes: dit_attn_workspace_size variant 3.
+ * Otherwise as dit_attn_forward_ws.
+ */
+int dit_attn_forward_qnorm(const void* q, const void* k, const void* v, void* out, int B, int H,
+                           int Lq, int Lk, int d, float scale, const void* q_weight, float eps,
+                           void* workspace, long long workspace_bytes, void* stream);
 
 /*
  * Per-tensor e4m3 quantisation (the prologue that gives dit_attn_forward_fp8
@@ -238,8 +285,11 @@ const char* dit_attn_status_string(int status);
 
 /*
  * Synchronise `stream`, then read and clear the device error word that the
- * kernels set when a bounded wait gives up.  Returns OK or TIMEOUT (or CUDA
- * if the synchronisation itself failed).  A test and debugging aid.
+ * kernels set when a bounded wait gives up.  The read and the clear are one
+ * atomic exchange on the device (a one-thread kernel on `stream`), so a
+ * TIMEOUT recorded meanwhile by a kernel on another stream is kept for the
+ * next call, never lost; concurrent callers are serialised.  Returns OK or
+ * TIMEOUT (or CUDA if a CUDA call failed).  A test and debugging aid.
  */
 int dit_attn_get_device_error(void* stream);
 
@@ -252,6 +302,23 @@ int dit_attn_get_device_error(void* stream);
  * usable.  Nothing faults or hangs.  Requires dit_attn_create().
  */
 int dit_attn_check_wait_timeout(int limit_us, void* stream);
+
+/*
+ * Self-test of the exponential the softmax evaluates on the FMA pipe for part
+ * of its probabilities (a Cody-Waite reduction and a minimax polynomial; the
+ * pages specify no exponential, so this is an implementation check, not a
+ * step of the method):
+ *
+ *     y_fma[i]  = the FMA-pipe 2^x[i] of the given degree (2: the e4m3-P
+ *                 softmax, 3: the bf16-P softmax), x clamped to [-125, 127]
+ *     y_mufu[i] = ex2.approx.ftz(x[i]), the MUFU instruction it stands in for
+ *
+ * x, y_fma, y_mufu: device fp32 [n], 4-byte aligned, not overlapping;
+ * 1 <= n <= 2^40; degree 2 or 3 (else INVALID_ARG).  Enqueued on `stream`;
+ * requires dit_attn_create().
+ */
+int dit_attn_check_exp2(const void* x, void* y_fma, void* y_mufu, long long n, int degree,
+                        void* stream);
 
 /* The cudaError_t behind the most recent DIT_ATTN_ERR_CUDA on this thread. */
 int dit_attn_last_cuda_error(void);

@@ -67,7 +67,8 @@ MB = 1 << 20
     ((A, A + MB, A + 2 * MB, A + 3 * MB + 2, 1, 1, 8, 8, 64, 0.125), 1),        # misaligned out
     ((A, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 8, 8, 64, float("nan")), 1),     # NaN scale
     ((A, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 8, 8, 64, float("inf")), 1),     # inf scale
-    ((A, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 8, 8, 64, -0.5), 1),             # negative scale
+    ((A, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 8, 8, 64, 2.4e38), 1),           # scale*log2(e) > FLT_MAX
+    ((A, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 8, 8, 64, -2.4e38), 1),
     ((A, A + MB, A + 2 * MB, A + 512, 1, 1, 8, 8, 64, 0.125), 1),               # out overlaps q
     ((A, A + MB, A + 2 * MB, A + MB + 512, 1, 1, 8, 8, 64, 0.125), 1),          # out overlaps k
     ((A, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 8, 8, 96, 0.125), 2),            # d = 96
@@ -77,6 +78,16 @@ MB = 1 << 20
 ])
 def test_forward_rejects_bad_arguments(args, expect):
     assert dit.forward_ptr(*args) == expect
+
+
+@pytest.mark.skipif(_has_gpu(), reason="a valid call with fake pointers must not reach a GPU")
+@pytest.mark.parametrize("scale", [-0.5, 0.0, -2.3e38, 2.3e38, -1e-30])
+def test_forward_accepts_every_usable_scale(scale):
+    # softmax(scale * q k^T) v is defined for any finite scale; every sign
+    # passes the argument checks (the call then stops at the device check)
+    assert dit.forward_ptr(A, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 8, 8, 128, scale) == 4
+    assert dit.forward_qk8_ptr(*_qk8(scale=scale, q_scale=1.0, k_scale=1.0)) == 4
+    assert dit.forward_fp8_ptr(*_fp8(scale=scale, q_scale=1.0, k_scale=1.0)) == 4
 
 
 @pytest.mark.skipif(_has_gpu(), reason="checks the no-device path")
@@ -144,6 +155,8 @@ def _qk8(**change):
     (_qk8(k_scale=-1.0), 1),                          # negative k_scale
     (_qk8(k_scale=float("inf")), 1),                  # inf k_scale
     (_qk8(scale=1e20, q_scale=1e20, k_scale=1e20), 1),  # combined scale overflows fp32
+    (_qk8(scale=-1e20, q_scale=1e20, k_scale=1e20), 1),
+    (_qk8(scale=2.4e36, q_scale=10.0, k_scale=10.0), 1),  # combined scale * log2(e) > FLT_MAX
     (_qk8(out=A + 512), 1),                           # out overlaps the 1 KB of q8
     (_qk8(d=64), 2),                                  # e4m3 path is d = 128 only
     (_qk8(d=96), 2),
@@ -254,6 +267,7 @@ def _fp8(**change):
     (_fp8(v_scale=1e-45), 1),                         # 1 / v_scale overflows fp32
     (_fp8(q_scale=-1.0), 1),
     (_fp8(scale=1e20, q_scale=1e20, k_scale=1e20), 1),
+    (_fp8(scale=-2.4e36, q_scale=10.0, k_scale=10.0), 1),
     (_fp8(out=A + 2 * MB + 512), 1),                  # out overlaps the 1 KB of v8
     (_fp8(d=64), 2),                                  # d = 128 only
     (_fp8(B=65536, H=65536), 2),
@@ -299,7 +313,7 @@ def test_workspace_size_variants_validate_before_cuda():
     lib = ctypes.CDLL(dit.library_path())
     lib.dit_attn_workspace_size.argtypes = [ctypes.c_int] * 6 + [ctypes.c_void_p]
     nb = ctypes.c_longlong(7)
-    assert lib.dit_attn_workspace_size(1, 1, 8, 8, 128, 3, ctypes.byref(nb)) == 1 and nb.value == 0
+    assert lib.dit_attn_workspace_size(1, 1, 8, 8, 128, 4, ctypes.byref(nb)) == 1 and nb.value == 0
     assert lib.dit_attn_workspace_size(1, 1, 8, 8, 128, -1, ctypes.byref(nb)) == 1
     assert lib.dit_attn_workspace_size(1, 1, 8, 8, 64, 2, ctypes.byref(nb)) == 2   # d = 128 only
 
@@ -314,3 +328,48 @@ def test_python_fp8_wrappers_check_tensors():
         dit.forward_fp8(x8, x8, x8, 1.0, 1.0, 1.0)         # CPU tensors
     with pytest.raises(TypeError):
         dit.quantize_e4m3(x, 1.0)                          # CPU tensor
+
+
+def test_check_exp2_validates_before_cuda():
+    lib = ctypes.CDLL(dit.library_path())
+    lib.dit_attn_check_exp2.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_longlong, ctypes.c_int,
+                                                                ctypes.c_void_p]
+    assert lib.dit_attn_check_exp2(None, A + MB, A + 2 * MB, 8, 3, None) == 1      # null x
+    assert lib.dit_attn_check_exp2(A, A + MB, A + 2 * MB, 0, 3, None) == 1         # n = 0
+    assert lib.dit_attn_check_exp2(A, A + MB, A + 2 * MB, 8, 4, None) == 1         # degree 4
+    assert lib.dit_attn_check_exp2(A + 2, A + MB, A + 2 * MB, 8, 3, None) == 1     # misaligned
+    assert lib.dit_attn_check_exp2(A, A + 16, A + 2 * MB, 8, 3, None) == 1         # overlap
+
+
+# ----------------------------------------------------------------- forward with the fused query norm
+
+QN = (A, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 8, 8, 128, 0.125, 0, 1e-6, 0, 0)
+
+
+def _qn(**change):
+    names = ("q", "k", "v", "out", "B", "H", "Lq", "Lk", "d", "scale", "q_weight", "eps",
+             "workspace", "workspace_bytes")
+    args = dict(zip(names, QN))
+    args.update(change)
+    return tuple(args[n] for n in names)
+
+
+@pytest.mark.parametrize("args,expect", [
+    (_qn(q=0), 1),                                    # null q
+    (_qn(eps=-1.0), 1),                               # negative eps
+    (_qn(eps=float("nan")), 1),
+    (_qn(q_weight=A + 4 * MB + 8), 1),                # misaligned weight
+    (_qn(q_weight=A + 3 * MB + 64), 1),               # weight inside out
+    (_qn(scale=float("inf")), 1),
+    (_qn(workspace=A + 4 * MB + 8, workspace_bytes=4096), 1),   # misaligned workspace
+    (_qn(d=64), 2),                                   # d = 128 only
+    (_qn(B=65536, H=65536), 2),
+])
+def test_forward_qnorm_rejects_bad_arguments(args, expect):
+    assert dit.forward_qnorm_ptr(*args) == expect
+
+
+@pytest.mark.skipif(_has_gpu(), reason="a valid call with fake pointers must not reach a GPU")
+def test_forward_qnorm_no_device():
+    assert dit.forward_qnorm_ptr(*QN) == 4
+    assert dit.forward_qnorm_ptr(*_qn(q_weight=A + 4 * MB, scale=-0.3)) == 4

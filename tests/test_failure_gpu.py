@@ -33,3 +33,23 @@ def test_bounded_wait_times_out_and_context_survives():
     torch.cuda.synchronize()
     assert dit.get_device_error() == 0
     assert_close(to_host_f64(out), oracle_full(q, k, v, 0.088), "after timeout")
+
+
+def test_timeout_recorded_while_another_stream_reads_is_kept():
+    # The read-and-clear of the error word is one atomic exchange: a TIMEOUT
+    # that a kernel on stream s1 records while dit_attn_get_device_error runs
+    # on an idle stream s2 is reported exactly once, never lost.
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import diffusion_transformer_joint_causal_b300 as dit
+    dit.create()
+    assert dit.get_device_error() == 0
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    seen = []
+    assert dit.check_wait_timeout(50000, s1) == 0      # gives up after 50 ms
+    for _ in range(200):
+        seen.append(dit.get_device_error(s2))
+    seen.append(dit.get_device_error(s1))               # waits for the s1 kernel
+    seen.append(dit.get_device_error(s2))
+    assert seen.count(6) == 1 and all(x in (0, 6) for x in seen), seen

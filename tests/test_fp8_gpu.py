@@ -338,3 +338,17 @@ def test_million_key_rows_fp8(dit):
     want = oracle.attention_rows(qd, kd, vd, scale, bh, rows)
     wabs = oracle.attention_rows(qd, kd, np.abs(vd), scale, bh, rows)
     assert_fp8_close(got[0, 0][rows], want, wabs, "2^20 keys, e4m3")
+
+
+def test_negative_scale(dit):
+    # either sign of the logit scale: against the oracle under the e4m3-P
+    # bound, and bit for bit against the positive scale with negated key codes
+    import torch
+    rng = np.random.default_rng(68)
+    q8, qs, qd = quantise(W.random_bf16(rng, (1, 3, 1000, 128)))
+    k8, ks, kd = quantise(W.random_bf16(rng, (1, 3, 1300, 128)))
+    v8, vs, vd = quantise(W.random_bf16(rng, (1, 3, 1300, 128)))
+    a = run_fp8(dit, q8, k8, v8, qs, ks, vs, -0.088)
+    check_full(to_host_f64(a), qd, kd, vd, -0.088, "e4m3 Q/K/V, negative scale")
+    b = run_fp8(dit, q8, k8 ^ np.uint8(0x80), v8, qs, ks, vs, 0.088)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))

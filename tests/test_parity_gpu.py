@@ -309,3 +309,99 @@ def test_million_key_rows(dit):
     rows = np.concatenate([np.arange(0, Lq, 8), [Lq - 1]])
     bh = np.zeros_like(rows)
     assert_close(got[0, 0][rows], oracle_sampled(q, k, v, scale, bh, rows), "2^20 keys")
+
+
+# ----------------------------------------------------------------- the literal C-ABI forward
+# dit_attn_forward(q, k, v, out, B, H, Lq, Lk, d, scale, stream) itself, with
+# raw device pointers and no workspace (the Python forward goes through the
+# workspace entry point).
+
+def _forward_literal(dit, qd, kd, vd, scale):
+    import torch
+    B, H, Lq, d = qd.shape
+    Lk = kd.shape[2]
+    out = torch.empty_like(qd)
+    rc = dit.forward_ptr(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), out.data_ptr(), B, H, Lq,
+                         Lk, d, scale, torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, dit.status_string(rc)
+    torch.cuda.synchronize()
+    assert dit.get_device_error() == 0
+    return out
+
+
+def test_literal_forward_tiny_every_element(dit):
+    w = W.workload("tiny")
+    q, k, v = W.make_qkv(w)
+    out = _forward_literal(dit, to_device(q), to_device(k), to_device(v), w.scale)
+    assert_close(to_host_f64(out), oracle_full(q, k, v, w.scale), "dit_attn_forward tiny")
+
+
+def test_literal_forward_ragged_outliers_sampled(dit):
+    import torch
+    w = W.workload("ragged_outliers")
+    q, k, v = W.make_qkv(w)
+    out = _forward_literal(dit, to_device(q), to_device(k), to_device(v), w.scale)
+    bh = np.repeat(np.arange(w.B * w.H), 256)
+    rows = np.concatenate([W.sample_rows(w, b, h) for b in range(w.B) for h in range(w.H)])
+    flat = out.view(w.B * w.H, w.Lq, w.d)
+    got = to_host_f64(flat[torch.from_numpy(bh).cuda(), torch.from_numpy(rows).cuda()])
+    assert_close(got, oracle_sampled(q, k, v, w.scale, bh, rows), "dit_attn_forward ragged")
+
+
+# ----------------------------------------------------------------- negative scales
+# softmax(scale * q k^T) v is defined for either sign of the scale; with
+# scale < 0 the row max of the scaled logits is scale times the row minimum
+# of q k^T.
+
+NEG_SHAPES = [(1, 2, 300, 389, 64), (2, 3, 129, 300, 64), (1, 2, 300, 389, 128),
+              (1, 3, 1000, 1000, 128), (1, 1, 1, 1, 128)]
+
+
+@pytest.mark.parametrize("shape", NEG_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_negative_scale_every_element(dit, shape):
+    B, H, Lq, Lk, d = shape
+    rng = np.random.default_rng(4000 + Lq + Lk + d)
+    q = W.random_bf16(rng, (B, H, Lq, d))
+    k = W.random_bf16(rng, (B, H, Lk, d))
+    v = W.random_bf16(rng, (B, H, Lk, d))
+    scale = float(np.float32(-1 / math.sqrt(d)))
+    got = to_host_f64(run(dit, q, k, v, scale))
+    assert_close(got, oracle_full(q, k, v, scale), f"negative scale {shape}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_negative_scale_large_logits(dit, d):
+    # logit spread far beyond exp's fp32 range, and a ragged key tail
+    rng = np.random.default_rng(4100 + d)
+    q = W.random_bf16(rng, (1, 2, 300, d), 4.0)
+    k = W.random_bf16(rng, (1, 2, 5000, d), 4.0)
+    v = W.random_bf16(rng, (1, 2, 5000, d))
+    got = to_host_f64(run(dit, q, k, v, -0.5))
+    assert_close(got, oracle_full(q, k, v, -0.5), f"negative scale, large logits, d={d}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_negative_scale_equals_negated_keys(dit, d):
+    # q (-k)^T = -(q k^T) exactly (bf16 negation is exact and the products are
+    # summed in the same order), so forward(q, k, v, -s) and forward(q, -k, v, s)
+    # see identical fp32 logits and must agree bit for bit.
+    import torch
+    rng = np.random.default_rng(4200 + d)
+    q = W.random_bf16(rng, (2, 2, 700, d))
+    k = W.random_bf16(rng, (2, 2, 1300, d))
+    v = W.random_bf16(rng, (2, 2, 1300, d))
+    neg_k = k ^ np.uint16(0x8000)
+    a = run(dit, q, k, v, -0.11)
+    b = run(dit, q, neg_k, v, 0.11)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_negative_scale_split_tail(dit):
+    B, H, Lq, Lk, d = 1, 1, 700, 4000, 128
+    assert dit.workspace_size(B, H, Lq, Lk, d) > 0
+    rng = np.random.default_rng(4300)
+    q = W.random_bf16(rng, (B, H, Lq, d))
+    k = W.random_bf16(rng, (B, H, Lk, d))
+    v = W.random_bf16(rng, (B, H, Lk, d))
+    got = to_host_f64(run(dit, q, k, v, -0.088))
+    assert_close(got, oracle_full(q, k, v, -0.088), "negative scale, split tail")

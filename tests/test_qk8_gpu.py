@@ -261,3 +261,18 @@ def test_split_tail_e4m3(dit):
     got = to_host_f64(run_qk8(dit, q8, k8, v, qs, ks, 0.088))
     want = oracle.attention(qd, kd, W.bf16_to_f32(v).astype(np.float64), 0.088)
     assert_close(got, want, "e4m3 split tail")
+
+
+def test_negative_scale(dit):
+    # either sign of the logit scale: against the oracle, and bit for bit
+    # against the positive scale with every key code negated (sign bit 0x80)
+    import torch
+    rng = np.random.default_rng(36)
+    q8, qs, qd = quantise(W.random_bf16(rng, (1, 3, 1000, 128)))
+    k8, ks, kd = quantise(W.random_bf16(rng, (1, 3, 1300, 128)))
+    v = W.random_bf16(rng, (1, 3, 1300, 128))
+    a = run_qk8(dit, q8, k8, v, qs, ks, -0.088)
+    want = oracle.attention(qd, kd, W.bf16_to_f32(v).astype(np.float64), -0.088)
+    assert_close(to_host_f64(a), want, "e4m3 Q/K, negative scale")
+    b = run_qk8(dit, q8, k8 ^ np.uint8(0x80), v, qs, ks, 0.088)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
