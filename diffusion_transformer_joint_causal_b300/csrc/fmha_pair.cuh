@@ -677,7 +677,9 @@ __device__ void pair_qnorm_role(const Params& p, const Shared& sh) {
        i += static_cast<int>(num_clusters_x()), ++it) {
     for (int t = 0; t < 2; ++t) {
       const bool got = mbar_wait(sh.bar(T::kBarQFull + t), it & 1u, kWaitLimitNs, sh.abort);
-      if (!__all_sync(0xffffffffu, got)) { stuck_tile = t; break; }
+      // both warps take the same decision (a lone warp would wait at the
+      // named barrier below for ever)
+      if (!named_bar_and(1, 64, got)) { stuck_tile = t; break; }
       const uint32_t tile = sh.base + T::kOffQ + t * T::kQTileBytes;
 #pragma unroll 1
       for (int r0 = 0; r0 < kBM; r0 += 4) {
