@@ -86,7 +86,7 @@ def test_fused_norm_weight_negative_scale_and_unsplit(dit):
     for scale, ws in ((0.088, "auto"), (-0.11, None)):
         fused, two = _pipelines(dit, to_device(qb), to_device(kb), to_device(vb), scale, w, ws)
         assert torch.equal(fused.view(torch.int16), two.view(torch.int16))
-        want = _oracle_end_to_end(qb, kb, vb, scale, W.bf16_to_f32(wb).astype(np.float64))
+        want = _oracle_end_to_end(qb, kb, vb, scale, wb)
         assert_close(to_host_f64(fused), want, f"weighted, scale {scale}")
 
 
