@@ -643,33 +643,38 @@ __device__ void softmax_role_pair(const Params& p, const Shared& sh, uint32_t tm
 
 // ----------------------------------------------------------------- query normalisation (kNormQ)
 // Warps 18-19 of each CTA (64 threads): as each of this CTA's query tiles
-// lands, RMS-normalise its 128 rows in place in shared memory with exactly
-// the arithmetic of dit_attn_rmsnorm (16 lanes per row, 8 columns a lane,
-// fp32 sum of squares in the same order, xor-shuffle reduction, rsqrt, times
-// the weight, rounded to nearest-even bf16), make the writes visible to the
-// tensor cores (async proxy) and report the tile ready on the leader's
-// barrier with a cluster-scope release.  A query tile lands one or two key
-// tiles before the MMA warp needs it, so the pass stays off the MMA chain.
+// lands, RMS-normalise its 128 rows in place in shared memory, one thread per
+// row (two rows each), make the writes visible to the tensor cores (async
+// proxy) and report the tile ready on the leader's barrier with a
+// cluster-scope release.  The arithmetic is dit_attn_rmsnorm's, operation for
+// operation: per 8-column chunk c a sum of squares s_c by fused multiply-adds
+// in column order, the 16 chunk sums combined in the order of that kernel's
+// xor-shuffle reduction, rsqrt, then x * inv * weight rounded to bf16; the
+// normalised rows are therefore bit-identical to dit_attn_rmsnorm's.  A
+// query tile lands about one key tile before the MMA warp needs it.
+template <class T>
+__device__ __forceinline__ uint32_t q_chunk_addr(uint32_t tile, int r, int c) {
+  // 128-byte swizzle: 16-byte unit u of a 128-byte row r sits at unit u ^ (r mod 8)
+  return tile + (c >> 3) * T::kQBoxBytes + r * 128 + ((((c & 7) ^ (r & 7))) << 4);
+}
+
+__device__ __forceinline__ float chunk_sum_squares(uint4 v) {
+  const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float lo = __uint_as_float(vv[k] << 16), hi = __uint_as_float(vv[k] & 0xFFFF0000u);
+    ss = fmaf(lo, lo, ss);
+    ss = fmaf(hi, hi, ss);
+  }
+  return ss;
+}
+
 template <class T>
 __device__ void pair_qnorm_role(const Params& p, const Shared& sh) {
   const int tid = static_cast<int>(threadIdx.x) - 18 * 32;     // 0..63
-  const int lane = threadIdx.x & 31;
-  const int chunk = lane & 15;                                  // columns 8*chunk .. +7
-  const int row_in = (tid >> 5) * 2 + (lane >> 4);             // row within a step of 4
   const uint32_t ready_leader = mapa_shared(sh.bar(T::kBarQReady), 0);
-  float wf[8];
-  if (p.q_weight) {
-    const uint4 wv = reinterpret_cast<const uint4*>(p.q_weight)[chunk];
-    const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      wf[2 * i] = __uint_as_float(ww[i] << 16);
-      wf[2 * i + 1] = __uint_as_float(ww[i] & 0xFFFF0000u);
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) wf[i] = 1.f;
-  }
+  const uint4* wgt = reinterpret_cast<const uint4*>(p.q_weight);
   const float eps = p.q_eps;
   uint32_t it = 0;
   int stuck_tile = -1;   // the tile whose landing a give-up left unobserved
@@ -682,30 +687,31 @@ __device__ void pair_qnorm_role(const Params& p, const Shared& sh) {
       if (!named_bar_and(1, 64, got)) { stuck_tile = t; break; }
       const uint32_t tile = sh.base + T::kOffQ + t * T::kQTileBytes;
 #pragma unroll 1
-      for (int r0 = 0; r0 < kBM; r0 += 4) {
-        const int r = r0 + row_in;
-        // 128-byte swizzle: 16-byte unit c of a 128-byte row r sits at unit c ^ (r mod 8)
-        const uint32_t addr = tile + (chunk >> 3) * T::kQBoxBytes + r * 128 +
-                              ((((chunk & 7) ^ (r & 7))) << 4);
-        const uint4 v = ld_shared_v4(addr);
-        const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
-        float f[8];
-        float ss = 0.f;
+      for (int r = tid; r < kBM; r += 64) {
+        // a[k] = s_k + s_(k+8), then the xor-tree order of the 16-lane reduction
+        float a[8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          f[2 * k] = __uint_as_float(vv[k] << 16);
-          f[2 * k + 1] = __uint_as_float(vv[k] & 0xFFFF0000u);
-          ss = fmaf(f[2 * k], f[2 * k], ss);
-          ss = fmaf(f[2 * k + 1], f[2 * k + 1], ss);
-        }
+        for (int c = 0; c < 8; ++c) a[c] = chunk_sum_squares(ld_shared_v4(q_chunk_addr<T>(tile, r, c)));
 #pragma unroll
-        for (int off = 8; off > 0; off /= 2) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        for (int c = 8; c < 16; ++c)
+          a[c - 8] = a[c - 8] + chunk_sum_squares(ld_shared_v4(q_chunk_addr<T>(tile, r, c)));
+        const float ss = ((a[0] + a[4]) + (a[2] + a[6])) + ((a[1] + a[5]) + (a[3] + a[7]));
         const float inv = rsqrtf(ss * (1.f / T::D) + eps);
-        uint32_t o[4];
+#pragma unroll 4
+        for (int c = 0; c < 16; ++c) {
+          const uint32_t addr = q_chunk_addr<T>(tile, r, c);
+          const uint4 v = ld_shared_v4(addr);
+          const uint4 wv = wgt ? wgt[c] : make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u,
+                                                     0x3F803F80u);   // bf16 ones
+          const uint32_t vv[4] = {v.x, v.y, v.z, v.w}, ww[4] = {wv.x, wv.y, wv.z, wv.w};
+          uint32_t o[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          o[k] = pack_bf16x2(f[2 * k] * inv * wf[2 * k], f[2 * k + 1] * inv * wf[2 * k + 1]);
-        st_shared_v4(addr, make_uint4(o[0], o[1], o[2], o[3]));
+          for (int k = 0; k < 4; ++k)
+            o[k] = pack_bf16x2(__uint_as_float(vv[k] << 16) * inv * __uint_as_float(ww[k] << 16),
+                               __uint_as_float(vv[k] & 0xFFFF0000u) * inv *
+                                   __uint_as_float(ww[k] & 0xFFFF0000u));
+          st_shared_v4(addr, make_uint4(o[0], o[1], o[2], o[3]));
+        }
       }
       fence_proxy_async_shared();
       named_bar_sync(1, 64);
