@@ -681,7 +681,9 @@ __device__ void pair_qnorm_role(const Params& p, const Shared& sh) {
   for (int i = static_cast<int>(cluster_id_x()); i < p.num_items && stuck_tile < 0;
        i += static_cast<int>(num_clusters_x()), ++it) {
     for (int t = 0; t < 2; ++t) {
-      const bool got = mbar_wait(sh.bar(T::kBarQFull + t), it & 1u, kWaitLimitNs, sh.abort);
+      // most of a work unit passes before the next query tile lands: poll gently
+      const bool got =
+          mbar_wait_backoff(sh.bar(T::kBarQFull + t), it & 1u, kWaitLimitNs, sh.abort, 256);
       // both warps take the same decision (a lone warp would wait at the
       // named barrier below for ever)
       if (!named_bar_and(1, 64, got)) { stuck_tile = t; break; }
