@@ -128,7 +128,7 @@ def _load():
             lib.dit_attn_quantize_e4m3.argtypes = [vp, vp, ctypes.c_longlong, ctypes.c_float, vp]
             lib.dit_attn_forward_qnorm.restype = c_int
             lib.dit_attn_forward_qnorm.argtypes = [vp, vp, vp, vp, c_int, c_int, c_int, c_int,
-                                                   c_int, ctypes.c_float, vp, ctypes.c_float, vp,
+                                                   c_int, ctypes.c_float, ctypes.c_float, vp,
                                                    ctypes.c_longlong, vp]
             lib.dit_attn_check_exp2.restype = c_int
             lib.dit_attn_check_exp2.argtypes = [vp, vp, vp, ctypes.c_longlong, c_int, vp]
@@ -316,36 +316,32 @@ def forward(q, k, v, scale: float | None = None, out=None, stream=None, workspac
 
 
 def forward_qnorm_ptr(q: int, k: int, v: int, out: int, B: int, H: int, Lq: int, Lk: int, d: int,
-                      scale: float, q_weight: int, eps: float, workspace: int,
-                      workspace_bytes: int, stream=0) -> int:
+                      scale: float, eps: float, workspace: int, workspace_bytes: int,
+                      stream=0) -> int:
     """Raw C-ABI call of dit_attn_forward_qnorm with integer device pointers."""
     s = stream if isinstance(stream, ctypes.c_void_p) else ctypes.c_void_p(int(stream))
     return _load().dit_attn_forward_qnorm(ctypes.c_void_p(q), ctypes.c_void_p(k),
                                           ctypes.c_void_p(v), ctypes.c_void_p(out), B, H, Lq, Lk,
-                                          d, ctypes.c_float(scale),
-                                          ctypes.c_void_p(q_weight) if q_weight else None,
-                                          ctypes.c_float(eps), ctypes.c_void_p(workspace),
+                                          d, ctypes.c_float(scale), ctypes.c_float(eps),
+                                          ctypes.c_void_p(workspace),
                                           ctypes.c_longlong(workspace_bytes), s)
 
 
-def forward_qnorm(q, k, v, scale: float | None = None, q_weight=None, eps: float = 1e-6,
-                  out=None, stream=None, workspace="auto"):
-    """forward(rmsnorm(q, q_weight, eps), k, v, scale) with the query normalisation
-    inside the attention kernel (bit for bit the two-call result); d = 128."""
+def forward_qnorm(q, k, v, scale: float | None = None, eps: float = 1e-6, out=None, stream=None,
+                  workspace="auto"):
+    """forward() on un-normalised queries: softmax((q / rms(q)) k^T * scale) v, with
+    rms(q) = sqrt(mean(q^2, last dim) + eps) folded into each row's softmax scale
+    inside the kernel; d = 128.  k is used as given (normalise it with rmsnorm)."""
     import torch
     B, H, Lq, Lk, d = _check_qkv(q, k, v, (torch.bfloat16,))
     out = _out_like(out, q, (B, H, Lq, d))
-    if q_weight is not None and (q_weight.dtype != torch.bfloat16 or tuple(q_weight.shape) != (d,)
-                                 or not q_weight.is_contiguous() or q_weight.device != q.device):
-        raise ValueError("q_weight must be a contiguous bf16 [d] tensor on q's device")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     with torch.cuda.device(q.device):
         ws, ws_ptr, ws_bytes = _workspace(workspace, q.device, B, H, Lq, Lk, d, 3, stream)
         rc = forward_qnorm_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, Lq,
-                               Lk, d, float(scale),
-                               q_weight.data_ptr() if q_weight is not None else 0, float(eps),
-                               ws_ptr, ws_bytes, _stream_handle(stream))
+                               Lk, d, float(scale), float(eps), ws_ptr, ws_bytes,
+                               _stream_handle(stream))
     if rc:
         raise DitAttnError(rc, "dit_attn_forward_qnorm")
     return out

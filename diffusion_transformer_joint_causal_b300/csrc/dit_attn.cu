@@ -141,8 +141,7 @@ struct Params {
   float* part_ml;    // [chunk][512 rows][2] fp32: running max (log2 units), row sum
   float v_scale;     // e4m3 values: dequantisation scale of v (1 otherwise)
   float inv_v_scale; // 1 / v_scale
-  const __nv_bfloat16* q_weight;   // fused query RMS norm: weight [128] or null
-  float q_eps;                     // fused query RMS norm: epsilon
+  float q_eps;       // query RMS norm folded into the softmax scale: epsilon
 };
 
 // One work item: query block `qblock` of head `bh` against key tiles
@@ -844,7 +843,6 @@ int launch(const void* q, const void* k, const void* v, void* out, int64_t BH, i
   p.part_ml = nullptr;
   p.v_scale = 1.f;
   p.inv_v_scale = 1.f;
-  p.q_weight = nullptr;
   p.q_eps = 0.f;
   const int grid = p.num_units < num_sms ? p.num_units : num_sms;
   dit::fmha_fwd_kernel<D><<<grid, dit::kNumThreads, Traits<D>::kSmemBytes, stream>>>(tq, tk, tv, p);
@@ -905,12 +903,12 @@ SplitPlan plan_split(int64_t num_units, int n_kv, int max_pairs) {
 // scales; with kPV8, v holds e4m3 bytes too, dequantised by v_scale.  With a
 // workspace of at least the plan's size the last, partial wave runs split,
 // followed by the combine kernel on the same stream.
-// With kNormQ, q holds un-normalised bf16 queries that the kernel RMS-normalises
-// (weight q_weight or none, epsilon q_eps) before their first product.
+// With kNormQ, q holds un-normalised bf16 queries whose RMS norm (epsilon
+// q_eps) the kernel folds into each row's softmax scale.
 template <bool kQK8, bool kPV8, bool kNormQ = false>
 int launch_pair(const void* q, const void* k, const void* v, void* out, int64_t BH, int Lq, int Lk,
                 double scale, cudaStream_t stream, int max_pairs, void* ws, int64_t ws_bytes,
-                float v_scale = 1.f, const void* q_weight = nullptr, float q_eps = 0.f) {
+                float v_scale = 1.f, float q_eps = 0.f) {
   CUtensorMap tq, tk, tv;
   int rc;
   const int qk_bytes = kQK8 ? 1 : 2;
@@ -929,7 +927,6 @@ int launch_pair(const void* q, const void* k, const void* v, void* out, int64_t 
   p.scale_log2 = static_cast<float>(scale * 1.4426950408889634);
   p.v_scale = v_scale;
   p.inv_v_scale = 1.f / v_scale;
-  p.q_weight = static_cast<const __nv_bfloat16*>(q_weight);
   p.q_eps = q_eps;
   SplitPlan plan = plan_split(p.num_units, (Lk + dit::kBN - 1) / dit::kBN, max_pairs);
   if (plan.splits > 1 && (!ws || ws_bytes < plan.ws_bytes))
@@ -1201,14 +1198,11 @@ int dit_attn_forward_fp8(const void* q8, const void* k8, const void* v8, void* o
 }
 
 int dit_attn_forward_qnorm(const void* q, const void* k, const void* v, void* out, int B, int H,
-                           int Lq, int Lk, int d, float scale, const void* q_weight, float eps,
-                           void* workspace, long long workspace_bytes, void* stream) {
+                           int Lq, int Lk, int d, float scale, float eps, void* workspace,
+                           long long workspace_bytes, void* stream) {
   int rc = check_forward_args(q, k, v, out, B, H, Lq, Lk, d, scale, 2);
   if (rc != DIT_ATTN_OK) return rc;
   if (!std::isfinite(eps) || eps < 0.f) return DIT_ATTN_ERR_INVALID_ARG;
-  if (q_weight && ((reinterpret_cast<uintptr_t>(q_weight) & 15u) ||
-                   overlaps(q_weight, 2 * 128, out, static_cast<int64_t>(B) * H * Lq * d * 2)))
-    return DIT_ATTN_ERR_INVALID_ARG;
   if (d != 128) return DIT_ATTN_ERR_UNSUPPORTED;
   rc = check_workspace(workspace, workspace_bytes, q, k, v, out, B, H, Lq, Lk, d, 2);
   if (rc != DIT_ATTN_OK) return rc;
@@ -1223,7 +1217,7 @@ int dit_attn_forward_qnorm(const void* q, const void* k, const void* v, void* ou
   }
   return launch_pair<false, false, true>(q, k, v, out, BH, Lq, Lk, scale,
                                          static_cast<cudaStream_t>(stream), max_pairs, workspace,
-                                         workspace_bytes, 1.f, q_weight, eps);
+                                         workspace_bytes, 1.f, eps);
 }
 
 }  // extern "C"

@@ -53,6 +53,13 @@ constexpr int kPairLoadWarp = 17;
 constexpr int kPairRegsSoftmax = 112;
 constexpr int kPairRegsOther = 32;
 
+// Split release of P: each query tile's probabilities go to the MMA warp in
+// two halves, the first 32-key chunk of every half-row (keys 0-31 and 64-95 of
+// the tile) as soon as it is stored, the second when the step ends, so that
+// half of the tile's P.V product runs while the softmax still works on the
+// second chunk.
+constexpr bool kSplitPRelease = true;
+
 // e4m3 probabilities: p = 2^(x - m + kProbOffsetE4M3) with the lazy rescale at
 // kRescaleThresholdE4M3, so p <= 2^8 after a max pass; an optimistic pass is
 // kept while its rounded row sum stays below 448 (no value saturated).  With
@@ -88,12 +95,13 @@ struct PairTraitsT {
   static constexpr int kBarQFull = 2 * kStages;      // leader: both CTAs' query tile t landed
   static constexpr int kBarQEmpty = kBarQFull + 2;   // both
   static constexpr int kBarSFull = kBarQEmpty + 2;   // both
-  static constexpr int kBarPFull = kBarSFull + 2;    // leader: 16 warp arrivals
-  static constexpr int kBarOFull = kBarPFull + 2;    // both
+  static constexpr int kBarPFull = kBarSFull + 2;    // leader: P (its first chunk when split) ready, 16 arrivals
+  static constexpr int kBarPFullB = kBarPFull + 2;   // leader: second chunk of P ready (split release)
+  static constexpr int kBarPVADone = kBarPFullB + 2; // both: P.V of the first chunk done (split release)
+  static constexpr int kBarOFull = kBarPVADone + 2;  // both
   static constexpr int kBarDrain = kBarOFull + 2;    // leader
   static constexpr int kBarProdDone = kBarDrain + 1; // leader: both producers reported
-  static constexpr int kBarQReady = kBarProdDone + 1;// leader: both CTAs' tile t normalised (2)
-  static constexpr int kNumBars = kBarQReady + 2;
+  static constexpr int kNumBars = kBarProdDone + 1;
   static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = 1024 + kOffMisc + kMiscWords * 4;
   static constexpr uint32_t kPFullArrivals = 16;     // 8 softmax warps x 2 CTAs
@@ -101,9 +109,7 @@ struct PairTraitsT {
 using PairTraits = PairTraitsT<false>;
 
 // ----------------------------------------------------------------- producer (both CTAs)
-// With kNormQ each CTA's query tile completes on the CTA's own barrier (its
-// own normalisation warps wait for it); otherwise on the leader's.
-template <bool kQK8, bool kPV8, bool kNormQ>
+template <bool kQK8, bool kPV8>
 __device__ void pair_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
                                const CUtensorMap* tmV, const Params& p, const Shared& sh) {
   using T = PairTraitsT<kQK8, kPV8>;
@@ -123,17 +129,10 @@ __device__ void pair_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
   auto load_q = [&](int t, int bh, int row0) -> bool {
     if (!mbar_wait(sh.bar(T::kBarQEmpty + t), (it & 1u) ^ 1u, kWaitLimitNs, sh.abort)) return false;
     const uint32_t dst = sh.base + T::kOffQ + t * T::kQTileBytes;
-    if constexpr (kNormQ) {
-      mbar_arrive_expect_tx(sh.bar(T::kBarQFull + t), T::kQTileBytes);
-      for (int b = 0; b < T::kQKBoxes; ++b)
-        tma_load_3d(dst + b * T::kQBoxBytes, tmQ, sh.bar(T::kBarQFull + t), b * T::kBoxCols,
-                    row0 + t * kBM, bh, pol_q);
-    } else {
-      if (leader) mbar_arrive_expect_tx(sh.bar(T::kBarQFull + t), 2 * T::kQTileBytes);
-      for (int b = 0; b < T::kQKBoxes; ++b)
-        tma_load_3d_pair(dst + b * T::kQBoxBytes, tmQ, qfull0_leader + 8u * t, b * T::kBoxCols,
-                         row0 + t * kBM, bh, pol_q);
-    }
+    if (leader) mbar_arrive_expect_tx(sh.bar(T::kBarQFull + t), 2 * T::kQTileBytes);
+    for (int b = 0; b < T::kQKBoxes; ++b)
+      tma_load_3d_pair(dst + b * T::kQBoxBytes, tmQ, qfull0_leader + 8u * t, b * T::kBoxCols,
+                       row0 + t * kBM, bh, pol_q);
     if (t == 0) ++q_loads0;
     else ++q_loads1;
     return true;
@@ -203,7 +202,7 @@ __device__ void pair_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
 // phase: where only the leader issued the fill it retires the missing half's
 // bytes itself (mbarrier.complete_tx), where only the peer did it arms the
 // phase for that half alone; then it waits (bounded) for the phase.
-template <class T, bool kNormQ>
+template <class T>
 __device__ void pair_teardown_drain(const Shared& sh) {
   const volatile int no_abort = 0;
   if (!mbar_wait_acquire_cluster(sh.bar(T::kBarProdDone), 0, kWaitLimitNs)) return;
@@ -225,10 +224,8 @@ __device__ void pair_teardown_drain(const Shared& sh) {
                      static_cast<int32_t>(f - fl) < 0, static_cast<int32_t>(f - fp) < 0,
                      (f & 1u) ? T::kVHalfBytes : T::kKHalfBytes, (f / T::kStages) & 1u);
   }
-  // query tiles: the two producers' load counts differ by at most one (with
-  // kNormQ each CTA's tiles complete locally and its normalisation warps
-  // drain them)
-  for (int t = 0; t < 2 && !kNormQ; ++t) {
+  // query tiles: the two producers' load counts differ by at most one
+  for (int t = 0; t < 2; ++t) {
     const uint32_t ql = word(kMiscQLoads + t), qp = word(kMiscPeerQLoads + t);
     const uint32_t q_last = static_cast<int32_t>(qp - ql) > 0 ? qp : ql;
     if (q_last == 0) continue;
@@ -282,7 +279,35 @@ __device__ __forceinline__ void pair_issue_pv(uint32_t d_tmem, uint32_t p_tmem, 
   }
 }
 
-template <bool kQK8, bool kPV8, bool kNormQ>
+// Half of a tile's P.V product: part 0 takes the keys of each half-row's
+// first 32-key chunk (tile keys 0-31 and 64-95), part 1 the others.
+template <bool kPV8, int kPart>
+__device__ __forceinline__ void pair_issue_pv_part(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_lo,
+                                                   bool accumulate) {
+  if constexpr (kPV8) {
+    constexpr uint32_t idesc = idesc_e4m3_f32(2 * kBM, PairTraits::D, 0, 1);
+    constexpr uint32_t hi = desc_hi_sw64(512);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int k = 2 * h + kPart;   // 32 keys per instruction
+      mma_ts_lo_pair_f8(d_tmem, p_tmem + (k / 2) * 64 + (k % 2) * 8, v_lo + ((k * 32 * 64) >> 4),
+                        hi, idesc, (accumulate || h > 0) ? 1u : 0u);
+    }
+  } else {
+    constexpr uint32_t idesc = idesc_bf16_f32(2 * kBM, PairTraits::D, 0, 1);
+    constexpr uint32_t hi = desc_hi_sw128(1024);
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        const int k = 4 * h + 2 * kPart + s;   // 16 keys per instruction
+        mma_ts_lo_pair(d_tmem, p_tmem + (k / 4) * 64 + (k % 4) * 8, v_lo + ((k * 16 * 128) >> 4),
+                       hi, idesc, (accumulate || h > 0 || s > 0) ? 1u : 0u);
+      }
+  }
+}
+
+template <bool kQK8, bool kPV8>
 __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) {
   using T = PairTraitsT<kQK8, kPV8>;
   constexpr uint16_t kBoth = 3;
@@ -304,15 +329,7 @@ __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) 
     if (++stage == T::kStages) { stage = 0; phase ^= 1u; }
     return true;
   };
-  // query tile t of this item in both CTAs' shared memory (normalised, with
-  // kNormQ: written by other threads, hence the cluster-scope acquire)
-  auto wait_q = [&](int t) -> bool {
-    if constexpr (kNormQ)
-      return __all_sync(0xffffffffu, mbar_wait_acquire_cluster(sh.bar(T::kBarQReady + t), it & 1u,
-                                                               kWaitLimitNs, sh.abort));
-    else
-      return wait(T::kBarQFull + t, it & 1u);
-  };
+  auto wait_q = [&](int t) -> bool { return wait(T::kBarQFull + t, it & 1u); };
 
   // Stage waits for the next key tile (its V and the following K) happen while
   // the warp waits for P_1 anyway, off the path from P-ready to the next MMA.
@@ -352,8 +369,21 @@ __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) 
       ok = wait(T::kBarPFull + 0, g & 1u);
       if (!ok) break;
       tc_fence_after();
+      if constexpr (kSplitPRelease) {
+        if (issuer) {
+          pair_issue_pv_part<kPV8, 0>(tmem + T::col_o(0), tmem + T::col_s(0), kv_lo(sV), j > 0);
+          mma_commit_pair(sh.bar(T::kBarPVADone + 0), kBoth);
+        }
+        __syncwarp();
+        ok = wait(T::kBarPFullB + 0, g & 1u);
+        if (!ok) break;
+        tc_fence_after();
+      }
       if (issuer) {
-        pair_issue_pv<kPV8>(tmem + T::col_o(0), tmem + T::col_s(0), kv_lo(sV), j > 0);
+        if constexpr (kSplitPRelease)
+          pair_issue_pv_part<kPV8, 1>(tmem + T::col_o(0), tmem + T::col_s(0), kv_lo(sV), true);
+        else
+          pair_issue_pv<kPV8>(tmem + T::col_o(0), tmem + T::col_s(0), kv_lo(sV), j > 0);
         if (more) {
           pair_issue_qk<kQK8>(tmem + T::col_s(0), q_lo0, kv_lo(sK_next));
           mma_commit_pair(sh.bar(T::kBarSFull + 0), kBoth);
@@ -367,8 +397,21 @@ __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) 
       ok = ok && wait(T::kBarPFull + 1, g & 1u);
       if (!ok) break;
       tc_fence_after();
+      if constexpr (kSplitPRelease) {
+        if (issuer) {
+          pair_issue_pv_part<kPV8, 0>(tmem + T::col_o(1), tmem + T::col_s(1), kv_lo(sV), j > 0);
+          mma_commit_pair(sh.bar(T::kBarPVADone + 1), kBoth);
+        }
+        __syncwarp();
+        ok = wait(T::kBarPFullB + 1, g & 1u);
+        if (!ok) break;
+        tc_fence_after();
+      }
       if (issuer) {
-        pair_issue_pv<kPV8>(tmem + T::col_o(1), tmem + T::col_s(1), kv_lo(sV), j > 0);
+        if constexpr (kSplitPRelease)
+          pair_issue_pv_part<kPV8, 1>(tmem + T::col_o(1), tmem + T::col_s(1), kv_lo(sV), true);
+        else
+          pair_issue_pv<kPV8>(tmem + T::col_o(1), tmem + T::col_s(1), kv_lo(sV), j > 0);
         if (more) {
           pair_issue_qk<kQK8>(tmem + T::col_s(1), q_lo1, kv_lo(sK_next));
           mma_commit_pair(sh.bar(T::kBarEmpty + sV), kBoth);
@@ -557,12 +600,155 @@ __device__ __forceinline__ void softmax_tile_lean(uint32_t taddr_s, int key0, bo
   l += sum8(acc);
 }
 
+// Sum of squares of this thread's half of query row r (64 bf16 values, in
+// column order) from a query tile in shared memory: two 128-byte-swizzled
+// boxes of 64 columns, 16-byte unit u of row r at unit u ^ (r mod 8).
+template <class T>
+__device__ __forceinline__ float q_half_row_sum_squares(uint32_t tile, int r, int half) {
+  const uint32_t row = tile + static_cast<uint32_t>(half) * T::kQBoxBytes + r * 128;
+  float ss = 0.f;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const uint4 v = ld_shared_v4(row + (((u ^ (r & 7))) << 4));
+    const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float lo = __uint_as_float(vv[k] << 16), hi = __uint_as_float(vv[k] & 0xFFFF0000u);
+      ss = fmaf(lo, lo, ss);
+      ss = fmaf(hi, hi, ss);
+    }
+  }
+  return ss;
+}
+
+// softmax_tile_lean with the split release of P: release(c) hands chunk c's
+// stored probabilities to the MMA warp (waits for the TMEM stores, arrives on
+// the chunk's P-ready barrier); wait_pv_a() waits until the first chunk's P.V
+// product has completed.  The row sum is accumulated exactly as in
+// softmax_tile_lean.  Optimistic pass: chunk 0 against the running max; if
+// its row sum overflows, the max pass runs before anything is released;
+// otherwise chunk 0 is released, and if chunk 1 then overflows, the max is
+// raised from chunk 1's logits (still in registers), O (which holds chunk 0's
+// product by then) and the row sum are rescaled, and chunk 1 is recomputed:
+// every key of the tile ends up weighed against one max.
+template <int D, bool kP8, class ORescale, class Release, class WaitPVA>
+__device__ __forceinline__ void softmax_tile_split(uint32_t taddr_s, int key0, bool first,
+                                                   bool masked, int valid, float scale_log2,
+                                                   float& m_used, float& l, ORescale&& o_rescale,
+                                                   Release&& release, WaitPVA&& wait_pv_a) {
+  constexpr int kPWords = kP8 ? 8 : 16;   // packed probability words per 32 keys
+  constexpr float kThreshold = kP8 ? kRescaleThresholdE4M3 : kRescaleThreshold;
+  uint32_t sr[32];
+  uint32_t pk[2 * kPWords];
+  float acc[8];
+  auto load = [&](int c) {
+    tmem_ld16x2_32<64>(taddr_s + 32 * c, sr);
+    tmem_wait_ld();
+  };
+  auto probs = [&](int c, float m) {
+    if constexpr (kP8) {
+      const float neg_m = kProbOffsetE4M3 - m;
+      if (masked) probs_chunk_e4m3<true>(sr, scale_log2, neg_m, key0 + 32 * c, valid, &pk[8 * c], acc);
+      else probs_chunk_e4m3<false>(sr, scale_log2, neg_m, key0 + 32 * c, kBN, &pk[8 * c], acc);
+    } else {
+      if (masked) probs_chunk<true>(sr, scale_log2, -m, key0 + 32 * c, valid, &pk[16 * c], acc);
+      else probs_chunk<false>(sr, scale_log2, -m, key0 + 32 * c, kBN, &pk[16 * c], acc);
+    }
+  };
+  auto store = [&](int c) {   // chunk c's P over its S columns (issued, not waited for)
+    if constexpr (kP8) tmem_st16x2_8<64>(taddr_s + 8 * c, &pk[8 * c]);
+    else tmem_st16x2_16<64>(taddr_s + 16 * c, &pk[16 * c]);
+  };
+  auto chunk_max = [&](int c) -> float {
+    return masked ? rowmax_chunk<true>(sr, key0 + 32 * c, valid, scale_log2)
+                  : rowmax_chunk<false>(sr, key0 + 32 * c, kBN, scale_log2);
+  };
+  auto clear = [&]() {
+#pragma unroll
+    for (int a = 0; a < 8; ++a) acc[a] = 0.f;
+  };
+  auto overflows = [&]() -> bool {   // warp-uniform: some row's sum so far is too large
+    const float half_sum = sum8(acc);
+    const float row_sum = half_sum + __shfl_xor_sync(0xffffffffu, half_sum, 16);
+    const bool big = kP8 ? !(row_sum < kOptimisticSumLimitE4M3) : !(row_sum <= kOptimisticSumLimit);
+    return __any_sync(0xffffffffu, big);
+  };
+  // Row max over both chunks (both still in TMEM), lazy rescale of l and O,
+  // the probabilities, both chunks released.
+  auto max_pass = [&]() {
+    load(0);
+    float mx = chunk_max(0);
+    load(1);
+    mx = fmaxf(mx, chunk_max(1));
+    const float m_tile = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    float factor = 1.f;
+    if (m_tile > m_used + kThreshold) {
+      factor = ex2_approx(m_used - m_tile);   // 0 on the first tile
+      l *= factor;
+      m_used = m_tile;
+    }
+    if (!first && __any_sync(0xffffffffu, factor != 1.f)) o_rescale(factor);
+    clear();
+    probs(1, m_used);
+    load(0);
+    probs(0, m_used);
+    store(0);
+    release(0);
+    store(1);
+    release(1);
+    l += sum8(acc);
+  };
+  clear();
+  if (first) {
+    max_pass();
+    return;
+  }
+  load(0);
+  probs(0, m_used);
+  if (overflows()) {
+    max_pass();
+    return;
+  }
+  const float l0 = sum8(acc);             // chunk 0's share, for a late rescale
+  store(0);
+  tmem_ld16x2_32<64>(taddr_s + 32, sr);   // chunk 1's logits, loaded while P0 is stored
+  release(0);
+  tmem_wait_ld();
+  probs(1, m_used);
+  if (overflows()) {
+    const float mx = chunk_max(1);
+    const float m_new = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    float factor = 1.f;
+    if (m_new > m_used + kThreshold) {
+      factor = ex2_approx(m_used - m_new);
+      m_used = m_new;
+    }
+    if (__any_sync(0xffffffffu, factor != 1.f)) {
+      wait_pv_a();          // O holds chunk 0's product before it is rescaled
+      o_rescale(factor);
+    }
+    l = (l + l0) * factor;   // chunk 0's share joins l; acc restarts with chunk 1
+    clear();
+    probs(1, m_used);
+  }
+  store(1);
+  release(1);
+  l += sum8(acc);
+}
+
 // Softmax and epilogue of the pair kernel: warp w works on query tile w / 8
 // and, with q = w mod 8, on TMEM lanes (rows) 32*(q%4) + 16*(q/4) .. +15, two
 // threads per row (lanes 0-15 take keys 0-63, lanes 16-31 keys 64-127).
 // Each warp arrives once per key tile on its tile's P-ready barrier of the
 // leader CTA (8 warps x 2 CTAs).
-template <int D, class T>
+// With kNormQ the queries arrive un-normalised: at the first key tile of each
+// work item (Q is then in shared memory, since its first product is done),
+// each thread reads its half of its row from the query tile, the two halves'
+// sums of squares are combined, and the row's softmax scale becomes
+// scale_log2 / sqrt(mean(q^2) + eps).  Since qn . k = (q . k) / sqrt(mean(q^2)
+// + eps), this is attention on RMS-normalised queries, without rounding the
+// normalised queries to bf16.
+template <int D, class T, bool kNormQ = false>
 __device__ void softmax_role_pair(const Params& p, const Shared& sh, uint32_t tmem) {
   const int warp = threadIdx.x / 32;                 // 0..15
   const int lane = threadIdx.x & 31;
@@ -580,6 +766,7 @@ __device__ void softmax_role_pair(const Params& p, const Shared& sh, uint32_t tm
   const int key0 = 64 * half;
   const int rank = static_cast<int>(cluster_ctarank());
   const uint32_t p_full_leader = mapa_shared(sh.bar(T::kBarPFull + t), 0);
+  const uint32_t p_full_b_leader = mapa_shared(sh.bar(T::kBarPFullB + t), 0);
   uint32_t g = 0, it = 0;
   bool ok = true;
 
@@ -588,20 +775,50 @@ __device__ void softmax_role_pair(const Params& p, const Shared& sh, uint32_t tm
     const WorkItem w = work_item(i, p, n_kv);
     float m_used = -INFINITY;   // running max, in units of s*scale*log2(e)
     float l = 0.f;              // this half-row's share of the row sum
+    float row_scale_log2 = scale_log2;
     for (int j = w.j0; j < w.j1 && ok; ++j, ++g) {
       const bool masked = (j == n_kv - 1) && (tail < kBN);
       const int valid = masked ? tail : kBN;
       const bool got = mbar_wait(sh.bar(T::kBarSFull + t), g & 1u, kWaitLimitNs, sh.abort);
       if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
       tc_fence_after();
+      if constexpr (kNormQ) {
+        if (j == w.j0) {
+          const float ss = q_half_row_sum_squares<T>(sh.base + T::kOffQ + t * T::kQTileBytes, r,
+                                                     half);
+          const float mean = (ss + __shfl_xor_sync(0xffffffffu, ss, 16)) * (1.f / D);
+          // an all-zero row (query rows past Lq) with eps = 0 has no norm: weigh its keys alike
+          const float inv = (mean > 0.f || p.q_eps > 0.f) ? rsqrtf(mean + p.q_eps) : 0.f;
+          row_scale_log2 = scale_log2 * inv;
+        }
+      }
       // O_t is quiescent here: S_t's completion implies the previous P.V
       // product into O_t finished.
-      softmax_tile_lean<D, T::kP8>(taddr_s, key0, j == w.j0, masked, valid, scale_log2, m_used,
-                                   l, [&](float f) { rescale_o_half<D>(taddr_o, f); });
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(p_full_leader);
+      if constexpr (kSplitPRelease) {
+        // the first-chunk P.V commit of this key tile; waited for only when a
+        // late max raise must rescale O
+        auto wait_pv_a = [&]() {
+          const bool done = mbar_wait(sh.bar(T::kBarPVADone + t), g & 1u, kWaitLimitNs, sh.abort);
+          if (!done) record_timeout<true>(sh);   // the next S wait gives up too
+          tc_fence_after();
+        };
+        auto release = [&](int c) {
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(c == 0 ? p_full_leader : p_full_b_leader);
+        };
+        softmax_tile_split<D, T::kP8>(taddr_s, key0, j == w.j0, masked, valid, row_scale_log2, m_used,
+                                      l, [&](float f) { rescale_o_half<D>(taddr_o, f); },
+                                      release, wait_pv_a);
+      } else {
+        softmax_tile_lean<D, T::kP8>(taddr_s, key0, j == w.j0, masked, valid, row_scale_log2, m_used,
+                                     l, [&](float f) { rescale_o_half<D>(taddr_o, f); });
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(p_full_leader);
+      }
     }
     if (!ok) break;
     // Epilogue: O_t / l -> bf16 -> global, each thread its D/2 columns; a
@@ -641,101 +858,10 @@ __device__ void softmax_role_pair(const Params& p, const Shared& sh, uint32_t tm
   if (!ok) record_timeout<true>(sh);
 }
 
-// ----------------------------------------------------------------- query normalisation (kNormQ)
-// Warps 18-19 of each CTA (64 threads): as each of this CTA's query tiles
-// lands, RMS-normalise its 128 rows in place in shared memory, one thread per
-// row (two rows each), make the writes visible to the tensor cores (async
-// proxy) and report the tile ready on the leader's barrier with a
-// cluster-scope release.  The arithmetic is dit_attn_rmsnorm's, operation for
-// operation: per 8-column chunk c a sum of squares s_c by fused multiply-adds
-// in column order, the 16 chunk sums combined in the order of that kernel's
-// xor-shuffle reduction, rsqrt, then x * inv * weight rounded to bf16; the
-// normalised rows are therefore bit-identical to dit_attn_rmsnorm's.  A
-// query tile lands about one key tile before the MMA warp needs it.
-template <class T>
-__device__ __forceinline__ uint32_t q_chunk_addr(uint32_t tile, int r, int c) {
-  // 128-byte swizzle: 16-byte unit u of a 128-byte row r sits at unit u ^ (r mod 8)
-  return tile + (c >> 3) * T::kQBoxBytes + r * 128 + ((((c & 7) ^ (r & 7))) << 4);
-}
-
-__device__ __forceinline__ float chunk_sum_squares(uint4 v) {
-  const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
-  float ss = 0.f;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float lo = __uint_as_float(vv[k] << 16), hi = __uint_as_float(vv[k] & 0xFFFF0000u);
-    ss = fmaf(lo, lo, ss);
-    ss = fmaf(hi, hi, ss);
-  }
-  return ss;
-}
-
-template <class T>
-__device__ void pair_qnorm_role(const Params& p, const Shared& sh) {
-  const int tid = static_cast<int>(threadIdx.x) - 18 * 32;     // 0..63
-  const uint32_t ready_leader = mapa_shared(sh.bar(T::kBarQReady), 0);
-  const uint4* wgt = reinterpret_cast<const uint4*>(p.q_weight);
-  const float eps = p.q_eps;
-  uint32_t it = 0;
-  int stuck_tile = -1;   // the tile whose landing a give-up left unobserved
-  for (int i = static_cast<int>(cluster_id_x()); i < p.num_items && stuck_tile < 0;
-       i += static_cast<int>(num_clusters_x()), ++it) {
-    for (int t = 0; t < 2; ++t) {
-      // most of a work unit passes before the next query tile lands: poll gently
-      const bool got =
-          mbar_wait_backoff(sh.bar(T::kBarQFull + t), it & 1u, kWaitLimitNs, sh.abort, 256);
-      // both warps take the same decision (a lone warp would wait at the
-      // named barrier below for ever)
-      if (!named_bar_and(1, 64, got)) { stuck_tile = t; break; }
-      const uint32_t tile = sh.base + T::kOffQ + t * T::kQTileBytes;
-#pragma unroll 1
-      for (int r = tid; r < kBM; r += 64) {
-        // a[k] = s_k + s_(k+8), then the xor-tree order of the 16-lane reduction
-        float a[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) a[c] = chunk_sum_squares(ld_shared_v4(q_chunk_addr<T>(tile, r, c)));
-#pragma unroll
-        for (int c = 8; c < 16; ++c)
-          a[c - 8] = a[c - 8] + chunk_sum_squares(ld_shared_v4(q_chunk_addr<T>(tile, r, c)));
-        const float ss = ((a[0] + a[4]) + (a[2] + a[6])) + ((a[1] + a[5]) + (a[3] + a[7]));
-        const float inv = rsqrtf(ss * (1.f / T::D) + eps);
-#pragma unroll 4
-        for (int c = 0; c < 16; ++c) {
-          const uint32_t addr = q_chunk_addr<T>(tile, r, c);
-          const uint4 v = ld_shared_v4(addr);
-          const uint4 wv = wgt ? wgt[c] : make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u,
-                                                     0x3F803F80u);   // bf16 ones
-          const uint32_t vv[4] = {v.x, v.y, v.z, v.w}, ww[4] = {wv.x, wv.y, wv.z, wv.w};
-          uint32_t o[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            o[k] = pack_bf16x2(__uint_as_float(vv[k] << 16) * inv * __uint_as_float(ww[k] << 16),
-                               __uint_as_float(vv[k] & 0xFFFF0000u) * inv *
-                                   __uint_as_float(ww[k] & 0xFFFF0000u));
-          st_shared_v4(addr, make_uint4(o[0], o[1], o[2], o[3]));
-        }
-      }
-      fence_proxy_async_shared();
-      named_bar_sync(1, 64);
-      if (tid == 0) mbar_arrive_release_cluster(ready_leader + 8u * static_cast<uint32_t>(t));
-    }
-  }
-  if (stuck_tile >= 0) {
-    if (tid == 0) {
-      record_timeout<true>(sh);
-      // copies of this item's query tiles may still be in flight: let them land
-      const volatile int no_abort = 0;
-      for (int t = stuck_tile; t < 2; ++t)
-        mbar_wait(sh.bar(T::kBarQFull + t), it & 1u, kWaitLimitNs, &no_abort);
-    }
-    __syncwarp();
-  }
-}
-
 // ----------------------------------------------------------------- kernel
 // Launched with a cluster dimension of 2 (consecutive CTAs form a pair).
-// kNormQ (bf16 only): queries arrive un-normalised and warps 18-19
-// RMS-normalise each tile in shared memory before its first product.
+// kNormQ (bf16 only): queries arrive un-normalised; their RMS norm is folded
+// into each row's softmax scale (softmax_role_pair).
 template <bool kQK8, bool kPV8, bool kNormQ = false>
 __global__ void __launch_bounds__(kPairThreads, 1)
     fmha_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -767,11 +893,12 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       mbar_init(sh.bar(T::kBarQEmpty + t), 1);
       mbar_init(sh.bar(T::kBarSFull + t), 1);
       mbar_init(sh.bar(T::kBarPFull + t), T::kPFullArrivals);
+      mbar_init(sh.bar(T::kBarPFullB + t), T::kPFullArrivals);
+      mbar_init(sh.bar(T::kBarPVADone + t), 1);
       mbar_init(sh.bar(T::kBarOFull + t), 1);
     }
     mbar_init(sh.bar(T::kBarDrain), 1);
     mbar_init(sh.bar(T::kBarProdDone), 2);
-    for (int t = 0; t < 2; ++t) mbar_init(sh.bar(T::kBarQReady + t), 2);
     *sh.abort = 0;
     fence_mbarrier_init();
   }
@@ -793,18 +920,17 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 
   if (warp < kPairMmaWarp) {
     reg_alloc<kPairRegsSoftmax>();
-    softmax_role_pair<T::D, T>(p, sh, tmem);
-    if (leader && threadIdx.x == 0 && *sh.abort) pair_teardown_drain<T, kNormQ>(sh);
+    softmax_role_pair<T::D, T, kNormQ>(p, sh, tmem);
+    if (leader && threadIdx.x == 0 && *sh.abort) pair_teardown_drain<T>(sh);
   } else if (warp == kPairMmaWarp) {
     reg_dealloc<kPairRegsOther>();
-    if (leader) pair_mma_role<kQK8, kPV8, kNormQ>(p, sh, tmem);
+    if (leader) pair_mma_role<kQK8, kPV8>(p, sh, tmem);
   } else if (warp == kPairLoadWarp) {
     reg_dealloc<kPairRegsOther>();
-    if (lane == 0) pair_load_role<kQK8, kPV8, kNormQ>(&tmQ, &tmK, &tmV, p, sh);
+    if (lane == 0) pair_load_role<kQK8, kPV8>(&tmQ, &tmK, &tmV, p, sh);
     __syncwarp();
   } else {
     reg_dealloc<kPairRegsOther>();
-    if constexpr (kNormQ) pair_qnorm_role<T>(p, sh);
   }
 
   // The leader drained its MMAs and, after a give-up, every copy either CTA

@@ -72,20 +72,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   }
 }
 
-// mbar_wait for a waiter that has nothing else to do for most of the wait:
-// between polls it sleeps sleep_ns, leaving its issue slots to the warps
-// that share its SM sub-partition.  Same limit and abort behaviour.
-__device__ __forceinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity, uint64_t limit_ns,
-                                                  const volatile int* abort, uint32_t sleep_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-    __nanosleep(sleep_ns);
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    if (globaltimer_ns() - t0 > limit_ns) return false;
-  }
-}
 
 // ----------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
@@ -203,6 +189,16 @@ __device__ __forceinline__ void tmem_ld16x2_32(uint32_t taddr, uint32_t (&r)[32]
 }
 
 template <int kOff>
+__device__ __forceinline__ void tmem_st16x2_8(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x32bx2.x8.b32 [%0], %1, "
+      "{%2, %3, %4, %5, %6, %7, %8, %9};" ::"r"(taddr),
+      "n"(kOff), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+      "r"(r[7])
+      : "memory");
+}
+
+template <int kOff>
 __device__ __forceinline__ void tmem_st16x2_16(uint32_t taddr, const uint32_t* r) {
   asm volatile(
       "tcgen05.st.sync.aligned.16x32bx2.x16.b32 [%0], %1, "
@@ -291,29 +287,6 @@ __device__ __forceinline__ bool mbar_wait_acquire_cluster(uint32_t bar, uint32_t
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
-// Make this thread's generic-proxy writes to shared memory visible to later
-// async-proxy reads (tensor-core operands, TMA).
-__device__ __forceinline__ void fence_proxy_async_shared() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-// Named barrier `id` over `count` threads (a multiple of 32).
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-// Named barrier `id` over `count` threads that also returns, to every one of
-// them, the AND of their predicates.
-__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t count, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, %2, %3, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
-      : "memory");
-  return r != 0;
-}
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -321,11 +294,6 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
                : "r"(addr)
                : "memory");
   return v;
-}
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
-  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
 }
 __device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
