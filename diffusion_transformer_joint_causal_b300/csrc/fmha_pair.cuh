@@ -53,13 +53,6 @@ constexpr int kPairLoadWarp = 17;
 constexpr int kPairRegsSoftmax = 112;
 constexpr int kPairRegsOther = 32;
 
-// Split release of P: each query tile's probabilities go to the MMA warp in
-// two halves, the first 32-key chunk of every half-row (keys 0-31 and 64-95 of
-// the tile) as soon as it is stored, the second when the step ends, so that
-// half of the tile's P.V product runs while the softmax still works on the
-// second chunk.
-constexpr bool kSplitPRelease = true;
-
 // e4m3 probabilities: p = 2^(x - m + kProbOffsetE4M3) with the lazy rescale at
 // kRescaleThresholdE4M3, so p <= 2^8 after a max pass; an optimistic pass is
 // kept while its rounded row sum stays below 448 (no value saturated).  With
@@ -95,10 +88,8 @@ struct PairTraitsT {
   static constexpr int kBarQFull = 2 * kStages;      // leader: both CTAs' query tile t landed
   static constexpr int kBarQEmpty = kBarQFull + 2;   // both
   static constexpr int kBarSFull = kBarQEmpty + 2;   // both
-  static constexpr int kBarPFull = kBarSFull + 2;    // leader: P (its first chunk when split) ready, 16 arrivals
-  static constexpr int kBarPFullB = kBarPFull + 2;   // leader: second chunk of P ready (split release)
-  static constexpr int kBarPVADone = kBarPFullB + 2; // both: P.V of the first chunk done (split release)
-  static constexpr int kBarOFull = kBarPVADone + 2;  // both
+  static constexpr int kBarPFull = kBarSFull + 2;    // leader: 16 warp arrivals
+  static constexpr int kBarOFull = kBarPFull + 2;    // both
   static constexpr int kBarDrain = kBarOFull + 2;    // leader
   static constexpr int kBarProdDone = kBarDrain + 1; // leader: both producers reported
   static constexpr int kNumBars = kBarProdDone + 1;
@@ -279,34 +270,6 @@ __device__ __forceinline__ void pair_issue_pv(uint32_t d_tmem, uint32_t p_tmem, 
   }
 }
 
-// Half of a tile's P.V product: part 0 takes the keys of each half-row's
-// first 32-key chunk (tile keys 0-31 and 64-95), part 1 the others.
-template <bool kPV8, int kPart>
-__device__ __forceinline__ void pair_issue_pv_part(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_lo,
-                                                   bool accumulate) {
-  if constexpr (kPV8) {
-    constexpr uint32_t idesc = idesc_e4m3_f32(2 * kBM, PairTraits::D, 0, 1);
-    constexpr uint32_t hi = desc_hi_sw64(512);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int k = 2 * h + kPart;   // 32 keys per instruction
-      mma_ts_lo_pair_f8(d_tmem, p_tmem + (k / 2) * 64 + (k % 2) * 8, v_lo + ((k * 32 * 64) >> 4),
-                        hi, idesc, (accumulate || h > 0) ? 1u : 0u);
-    }
-  } else {
-    constexpr uint32_t idesc = idesc_bf16_f32(2 * kBM, PairTraits::D, 0, 1);
-    constexpr uint32_t hi = desc_hi_sw128(1024);
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-      for (int s = 0; s < 2; ++s) {
-        const int k = 4 * h + 2 * kPart + s;   // 16 keys per instruction
-        mma_ts_lo_pair(d_tmem, p_tmem + (k / 4) * 64 + (k % 4) * 8, v_lo + ((k * 16 * 128) >> 4),
-                       hi, idesc, (accumulate || h > 0 || s > 0) ? 1u : 0u);
-      }
-  }
-}
-
 template <bool kQK8, bool kPV8>
 __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) {
   using T = PairTraitsT<kQK8, kPV8>;
@@ -369,21 +332,8 @@ __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) 
       ok = wait(T::kBarPFull + 0, g & 1u);
       if (!ok) break;
       tc_fence_after();
-      if constexpr (kSplitPRelease) {
-        if (issuer) {
-          pair_issue_pv_part<kPV8, 0>(tmem + T::col_o(0), tmem + T::col_s(0), kv_lo(sV), j > 0);
-          mma_commit_pair(sh.bar(T::kBarPVADone + 0), kBoth);
-        }
-        __syncwarp();
-        ok = wait(T::kBarPFullB + 0, g & 1u);
-        if (!ok) break;
-        tc_fence_after();
-      }
       if (issuer) {
-        if constexpr (kSplitPRelease)
-          pair_issue_pv_part<kPV8, 1>(tmem + T::col_o(0), tmem + T::col_s(0), kv_lo(sV), true);
-        else
-          pair_issue_pv<kPV8>(tmem + T::col_o(0), tmem + T::col_s(0), kv_lo(sV), j > 0);
+        pair_issue_pv<kPV8>(tmem + T::col_o(0), tmem + T::col_s(0), kv_lo(sV), j > 0);
         if (more) {
           pair_issue_qk<kQK8>(tmem + T::col_s(0), q_lo0, kv_lo(sK_next));
           mma_commit_pair(sh.bar(T::kBarSFull + 0), kBoth);
@@ -397,21 +347,8 @@ __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) 
       ok = ok && wait(T::kBarPFull + 1, g & 1u);
       if (!ok) break;
       tc_fence_after();
-      if constexpr (kSplitPRelease) {
-        if (issuer) {
-          pair_issue_pv_part<kPV8, 0>(tmem + T::col_o(1), tmem + T::col_s(1), kv_lo(sV), j > 0);
-          mma_commit_pair(sh.bar(T::kBarPVADone + 1), kBoth);
-        }
-        __syncwarp();
-        ok = wait(T::kBarPFullB + 1, g & 1u);
-        if (!ok) break;
-        tc_fence_after();
-      }
       if (issuer) {
-        if constexpr (kSplitPRelease)
-          pair_issue_pv_part<kPV8, 1>(tmem + T::col_o(1), tmem + T::col_s(1), kv_lo(sV), true);
-        else
-          pair_issue_pv<kPV8>(tmem + T::col_o(1), tmem + T::col_s(1), kv_lo(sV), j > 0);
+        pair_issue_pv<kPV8>(tmem + T::col_o(1), tmem + T::col_s(1), kv_lo(sV), j > 0);
         if (more) {
           pair_issue_qk<kQK8>(tmem + T::col_s(1), q_lo1, kv_lo(sK_next));
           mma_commit_pair(sh.bar(T::kBarEmpty + sV), kBoth);
@@ -621,121 +558,6 @@ __device__ __forceinline__ float q_half_row_sum_squares(uint32_t tile, int r, in
   return ss;
 }
 
-// softmax_tile_lean with the split release of P: release(c) hands chunk c's
-// stored probabilities to the MMA warp (waits for the TMEM stores, arrives on
-// the chunk's P-ready barrier); wait_pv_a() waits until the first chunk's P.V
-// product has completed.  The row sum is accumulated exactly as in
-// softmax_tile_lean.  Optimistic pass: chunk 0 against the running max; if
-// its row sum overflows, the max pass runs before anything is released;
-// otherwise chunk 0 is released, and if chunk 1 then overflows, the max is
-// raised from chunk 1's logits (still in registers), O (which holds chunk 0's
-// product by then) and the row sum are rescaled, and chunk 1 is recomputed:
-// every key of the tile ends up weighed against one max.
-template <int D, bool kP8, class ORescale, class Release, class WaitPVA>
-__device__ __forceinline__ void softmax_tile_split(uint32_t taddr_s, int key0, bool first,
-                                                   bool masked, int valid, float scale_log2,
-                                                   float& m_used, float& l, ORescale&& o_rescale,
-                                                   Release&& release, WaitPVA&& wait_pv_a) {
-  constexpr int kPWords = kP8 ? 8 : 16;   // packed probability words per 32 keys
-  constexpr float kThreshold = kP8 ? kRescaleThresholdE4M3 : kRescaleThreshold;
-  uint32_t sr[32];
-  uint32_t pk[2 * kPWords];
-  float acc[8];
-  auto load = [&](int c) {
-    tmem_ld16x2_32<64>(taddr_s + 32 * c, sr);
-    tmem_wait_ld();
-  };
-  auto probs = [&](int c, float m) {
-    if constexpr (kP8) {
-      const float neg_m = kProbOffsetE4M3 - m;
-      if (masked) probs_chunk_e4m3<true>(sr, scale_log2, neg_m, key0 + 32 * c, valid, &pk[8 * c], acc);
-      else probs_chunk_e4m3<false>(sr, scale_log2, neg_m, key0 + 32 * c, kBN, &pk[8 * c], acc);
-    } else {
-      if (masked) probs_chunk<true>(sr, scale_log2, -m, key0 + 32 * c, valid, &pk[16 * c], acc);
-      else probs_chunk<false>(sr, scale_log2, -m, key0 + 32 * c, kBN, &pk[16 * c], acc);
-    }
-  };
-  auto store = [&](int c) {   // chunk c's P over its S columns (issued, not waited for)
-    if constexpr (kP8) tmem_st16x2_8<64>(taddr_s + 8 * c, &pk[8 * c]);
-    else tmem_st16x2_16<64>(taddr_s + 16 * c, &pk[16 * c]);
-  };
-  auto chunk_max = [&](int c) -> float {
-    return masked ? rowmax_chunk<true>(sr, key0 + 32 * c, valid, scale_log2)
-                  : rowmax_chunk<false>(sr, key0 + 32 * c, kBN, scale_log2);
-  };
-  auto clear = [&]() {
-#pragma unroll
-    for (int a = 0; a < 8; ++a) acc[a] = 0.f;
-  };
-  auto overflows = [&]() -> bool {   // warp-uniform: some row's sum so far is too large
-    const float half_sum = sum8(acc);
-    const float row_sum = half_sum + __shfl_xor_sync(0xffffffffu, half_sum, 16);
-    const bool big = kP8 ? !(row_sum < kOptimisticSumLimitE4M3) : !(row_sum <= kOptimisticSumLimit);
-    return __any_sync(0xffffffffu, big);
-  };
-  // Row max over both chunks (both still in TMEM), lazy rescale of l and O,
-  // the probabilities, both chunks released.
-  auto max_pass = [&]() {
-    load(0);
-    float mx = chunk_max(0);
-    load(1);
-    mx = fmaxf(mx, chunk_max(1));
-    const float m_tile = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-    float factor = 1.f;
-    if (m_tile > m_used + kThreshold) {
-      factor = ex2_approx(m_used - m_tile);   // 0 on the first tile
-      l *= factor;
-      m_used = m_tile;
-    }
-    if (!first && __any_sync(0xffffffffu, factor != 1.f)) o_rescale(factor);
-    clear();
-    probs(1, m_used);
-    load(0);
-    probs(0, m_used);
-    store(0);
-    release(0);
-    store(1);
-    release(1);
-    l += sum8(acc);
-  };
-  clear();
-  if (first) {
-    max_pass();
-    return;
-  }
-  load(0);
-  probs(0, m_used);
-  if (overflows()) {
-    max_pass();
-    return;
-  }
-  const float l0 = sum8(acc);             // chunk 0's share, for a late rescale
-  store(0);
-  tmem_ld16x2_32<64>(taddr_s + 32, sr);   // chunk 1's logits, loaded while P0 is stored
-  release(0);
-  tmem_wait_ld();
-  probs(1, m_used);
-  if (overflows()) {
-    const float mx = chunk_max(1);
-    const float m_new = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-    float factor = 1.f;
-    if (m_new > m_used + kThreshold) {
-      factor = ex2_approx(m_used - m_new);
-      m_used = m_new;
-    }
-    if (__any_sync(0xffffffffu, factor != 1.f)) {
-      wait_pv_a();          // O holds chunk 0's product before it is rescaled
-      o_rescale(factor);
-    }
-    l = (l + l0) * factor;   // chunk 0's share joins l; acc restarts with chunk 1
-    clear();
-    probs(1, m_used);
-  }
-  store(1);
-  release(1);
-  l += sum8(acc);
-}
-
 // Softmax and epilogue of the pair kernel: warp w works on query tile w / 8
 // and, with q = w mod 8, on TMEM lanes (rows) 32*(q%4) + 16*(q/4) .. +15, two
 // threads per row (lanes 0-15 take keys 0-63, lanes 16-31 keys 64-127).
@@ -766,7 +588,6 @@ __device__ void softmax_role_pair(const Params& p, const Shared& sh, uint32_t tm
   const int key0 = 64 * half;
   const int rank = static_cast<int>(cluster_ctarank());
   const uint32_t p_full_leader = mapa_shared(sh.bar(T::kBarPFull + t), 0);
-  const uint32_t p_full_b_leader = mapa_shared(sh.bar(T::kBarPFullB + t), 0);
   uint32_t g = 0, it = 0;
   bool ok = true;
 
@@ -794,31 +615,12 @@ __device__ void softmax_role_pair(const Params& p, const Shared& sh, uint32_t tm
       }
       // O_t is quiescent here: S_t's completion implies the previous P.V
       // product into O_t finished.
-      if constexpr (kSplitPRelease) {
-        // the first-chunk P.V commit of this key tile; waited for only when a
-        // late max raise must rescale O
-        auto wait_pv_a = [&]() {
-          const bool done = mbar_wait(sh.bar(T::kBarPVADone + t), g & 1u, kWaitLimitNs, sh.abort);
-          if (!done) record_timeout<true>(sh);   // the next S wait gives up too
-          tc_fence_after();
-        };
-        auto release = [&](int c) {
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(c == 0 ? p_full_leader : p_full_b_leader);
-        };
-        softmax_tile_split<D, T::kP8>(taddr_s, key0, j == w.j0, masked, valid, row_scale_log2, m_used,
-                                      l, [&](float f) { rescale_o_half<D>(taddr_o, f); },
-                                      release, wait_pv_a);
-      } else {
-        softmax_tile_lean<D, T::kP8>(taddr_s, key0, j == w.j0, masked, valid, row_scale_log2, m_used,
-                                     l, [&](float f) { rescale_o_half<D>(taddr_o, f); });
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(p_full_leader);
-      }
+      softmax_tile_lean<D, T::kP8>(taddr_s, key0, j == w.j0, masked, valid, row_scale_log2, m_used,
+                                   l, [&](float f) { rescale_o_half<D>(taddr_o, f); });
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(p_full_leader);
     }
     if (!ok) break;
     // Epilogue: O_t / l -> bf16 -> global, each thread its D/2 columns; a
@@ -893,8 +695,6 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       mbar_init(sh.bar(T::kBarQEmpty + t), 1);
       mbar_init(sh.bar(T::kBarSFull + t), 1);
       mbar_init(sh.bar(T::kBarPFull + t), T::kPFullArrivals);
-      mbar_init(sh.bar(T::kBarPFullB + t), T::kPFullArrivals);
-      mbar_init(sh.bar(T::kBarPVADone + t), 1);
       mbar_init(sh.bar(T::kBarOFull + t), 1);
     }
     mbar_init(sh.bar(T::kBarDrain), 1);

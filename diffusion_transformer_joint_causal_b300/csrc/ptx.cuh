@@ -189,16 +189,6 @@ __device__ __forceinline__ void tmem_ld16x2_32(uint32_t taddr, uint32_t (&r)[32]
 }
 
 template <int kOff>
-__device__ __forceinline__ void tmem_st16x2_8(uint32_t taddr, const uint32_t* r) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.16x32bx2.x8.b32 [%0], %1, "
-      "{%2, %3, %4, %5, %6, %7, %8, %9};" ::"r"(taddr),
-      "n"(kOff), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
-      "r"(r[7])
-      : "memory");
-}
-
-template <int kOff>
 __device__ __forceinline__ void tmem_st16x2_16(uint32_t taddr, const uint32_t* r) {
   asm volatile(
       "tcgen05.st.sync.aligned.16x32bx2.x16.b32 [%0], %1, "
