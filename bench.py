@@ -507,42 +507,6 @@ def e4m3_sweep(dit, dev, peaks, bf16_ms: dict, calls: int = 20):
     return res["qk8"], res["fp8"]
 
 
-def qnorm_pipeline(dit, dev, q, k, v, w, calls: int = 20):
-    """Q and K RMS norm plus attention on the workload's tensors, two ways:
-    the separate prologue (dit.rmsnorm of Q and of K, then dit.forward) and
-    the fused query norm (dit.rmsnorm of K, then dit.forward_qnorm, which
-    normalises each query tile in shared memory).  Inputs are the workload's
-    tensors (normalising them again costs the same as normalising raw ones)."""
-    import torch
-    qn, kn, out = torch.empty_like(q), torch.empty_like(k), torch.empty_like(q)
-
-    def separate():
-        dit.rmsnorm(q, out=qn)
-        dit.rmsnorm(k, out=kn)
-        dit.forward(qn, kn, v, w.scale, out=out)
-
-    def fused():
-        dit.rmsnorm(k, out=kn)
-        dit.forward_qnorm(q, kn, v, w.scale, out=out)
-
-    res = {}
-    for _ in range(3):
-        separate()
-        fused()
-    torch.cuda.synchronize(dev)
-    for name, fn in (("ms_separate_prologue", separate), ("ms_fused_query_norm", fused)):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(calls):
-            fn()
-        e1.record()
-        torch.cuda.synchronize(dev)
-        res[name] = e0.elapsed_time(e1) / calls
-    res["saving"] = 1.0 - res["ms_fused_query_norm"] / res["ms_separate_prologue"]
-    res["launches"] = {"separate": 3, "fused": 2}
-    return res
-
-
 def v_calibration(v) -> float:
     """Per-tensor dequantisation scale of the values, max|V| / 448 (a static
     scale taken once, before any timed region, as a calibration pass would)."""
@@ -750,8 +714,6 @@ def bench_ours(args):
         line["rmsnorm_qk_prologue"] = rmsnorm_roofline(dit, dev, peaks)
         bf16_ms = {n: r["ms_eager"] for n, r in line["per_workload"].items()}
         line["qk8"], line["fp8"] = e4m3_sweep(dit, dev, peaks, bf16_ms)
-        if not qk8 and w.d == 128:
-            line["qnorm_pipeline"] = qnorm_pipeline(dit, dev, q, k, v, w)
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     print(json.dumps(line), flush=True)

@@ -33,7 +33,7 @@ __all__ = ["create", "destroy", "forward", "forward_ptr", "status_string", "get_
            "rmsnorm_e4m3", "rmsnorm_e4m3_ptr", "forward_ws_ptr", "forward_qk8_ws_ptr",
            "workspace_size", "forward_noalloc", "forward_noalloc_ptr", "forward_fp8",
            "forward_fp8_ptr", "forward_fp8_ws_ptr", "quantize_e4m3", "quantize_e4m3_ptr",
-           "check_exp2", "forward_qnorm", "forward_qnorm_ptr", "last_cuda_error", "version", "library_path", "DitAttnError", "STATUS",
+           "check_exp2", "last_cuda_error", "version", "library_path", "DitAttnError", "STATUS",
            "EXPORTED_SYMBOLS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -50,8 +50,7 @@ EXPORTED_SYMBOLS = ("dit_attn_version", "dit_attn_create", "dit_attn_forward",
                     "dit_attn_forward_qk8", "dit_attn_rmsnorm_e4m3", "dit_attn_forward_ws",
                     "dit_attn_forward_qk8_ws", "dit_attn_workspace_size",
                     "dit_attn_forward_noalloc", "dit_attn_forward_fp8",
-                    "dit_attn_forward_fp8_ws", "dit_attn_quantize_e4m3", "dit_attn_check_exp2",
-                    "dit_attn_forward_qnorm")
+                    "dit_attn_forward_fp8_ws", "dit_attn_quantize_e4m3", "dit_attn_check_exp2")
 
 _lock = threading.Lock()
 _lib = None
@@ -126,10 +125,6 @@ def _load():
                                                     ctypes.c_longlong, vp]
             lib.dit_attn_quantize_e4m3.restype = c_int
             lib.dit_attn_quantize_e4m3.argtypes = [vp, vp, ctypes.c_longlong, ctypes.c_float, vp]
-            lib.dit_attn_forward_qnorm.restype = c_int
-            lib.dit_attn_forward_qnorm.argtypes = [vp, vp, vp, vp, c_int, c_int, c_int, c_int,
-                                                   c_int, ctypes.c_float, ctypes.c_float, vp,
-                                                   ctypes.c_longlong, vp]
             lib.dit_attn_check_exp2.restype = c_int
             lib.dit_attn_check_exp2.argtypes = [vp, vp, vp, ctypes.c_longlong, c_int, vp]
             lib.dit_attn_last_cuda_error.restype = c_int
@@ -239,8 +234,7 @@ def _out_like(out, q, shape):
 def workspace_size(B: int, H: int, Lq: int, Lk: int, d: int, qk8: bool = False,
                    variant: int | None = None) -> int:
     """Bytes of split-tail workspace the forward uses for these sizes (0: none).
-    variant: 0 forward, 1 forward_qk8, 2 forward_fp8, 3 forward_qnorm
-    (default: 1 if qk8 else 0)."""
+    variant: 0 forward, 1 forward_qk8, 2 forward_fp8 (default: 1 if qk8 else 0)."""
     if variant is None:
         variant = 1 if qk8 else 0
     nb = ctypes.c_longlong(0)
@@ -312,38 +306,6 @@ def forward(q, k, v, scale: float | None = None, out=None, stream=None, workspac
                             _stream_handle(stream))
     if rc:
         raise DitAttnError(rc, "dit_attn_forward_ws")
-    return out
-
-
-def forward_qnorm_ptr(q: int, k: int, v: int, out: int, B: int, H: int, Lq: int, Lk: int, d: int,
-                      scale: float, eps: float, workspace: int, workspace_bytes: int,
-                      stream=0) -> int:
-    """Raw C-ABI call of dit_attn_forward_qnorm with integer device pointers."""
-    s = stream if isinstance(stream, ctypes.c_void_p) else ctypes.c_void_p(int(stream))
-    return _load().dit_attn_forward_qnorm(ctypes.c_void_p(q), ctypes.c_void_p(k),
-                                          ctypes.c_void_p(v), ctypes.c_void_p(out), B, H, Lq, Lk,
-                                          d, ctypes.c_float(scale), ctypes.c_float(eps),
-                                          ctypes.c_void_p(workspace),
-                                          ctypes.c_longlong(workspace_bytes), s)
-
-
-def forward_qnorm(q, k, v, scale: float | None = None, eps: float = 1e-6, out=None, stream=None,
-                  workspace="auto"):
-    """forward() on un-normalised queries: softmax((q / rms(q)) k^T * scale) v, with
-    rms(q) = sqrt(mean(q^2, last dim) + eps) folded into each row's softmax scale
-    inside the kernel; d = 128.  k is used as given (normalise it with rmsnorm)."""
-    import torch
-    B, H, Lq, Lk, d = _check_qkv(q, k, v, (torch.bfloat16,))
-    out = _out_like(out, q, (B, H, Lq, d))
-    if scale is None:
-        scale = 1.0 / math.sqrt(d)
-    with torch.cuda.device(q.device):
-        ws, ws_ptr, ws_bytes = _workspace(workspace, q.device, B, H, Lq, Lk, d, 3, stream)
-        rc = forward_qnorm_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, Lq,
-                               Lk, d, float(scale), float(eps), ws_ptr, ws_bytes,
-                               _stream_handle(stream))
-    if rc:
-        raise DitAttnError(rc, "dit_attn_forward_qnorm")
     return out
 
 

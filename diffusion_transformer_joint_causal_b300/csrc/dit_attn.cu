@@ -141,7 +141,6 @@ struct Params {
   float* part_ml;    // [chunk][512 rows][2] fp32: running max (log2 units), row sum
   float v_scale;     // e4m3 values: dequantisation scale of v (1 otherwise)
   float inv_v_scale; // 1 / v_scale
-  float q_eps;       // query RMS norm folded into the softmax scale: epsilon
 };
 
 // One work item: query block `qblock` of head `bh` against key tiles
@@ -764,7 +763,6 @@ struct DeviceState {
   int max_pairs = 0;       // co-resident clusters of two CTAs of the bf16 pair kernel
   int max_pairs_qk8 = 0;   // the same for the e4m3-QK pair kernel
   int max_pairs_fp8 = 0;   // the same for the e4m3 Q/K/V pair kernel
-  int max_pairs_qnorm = 0; // the same for the bf16 pair kernel with the fused query norm
   void* scratch = nullptr; // device address of g_scratch on this device
 };
 
@@ -843,7 +841,6 @@ int launch(const void* q, const void* k, const void* v, void* out, int64_t BH, i
   p.part_ml = nullptr;
   p.v_scale = 1.f;
   p.inv_v_scale = 1.f;
-  p.q_eps = 0.f;
   const int grid = p.num_units < num_sms ? p.num_units : num_sms;
   dit::fmha_fwd_kernel<D><<<grid, dit::kNumThreads, Traits<D>::kSmemBytes, stream>>>(tq, tk, tv, p);
   const cudaError_t e = cudaGetLastError();
@@ -903,12 +900,10 @@ SplitPlan plan_split(int64_t num_units, int n_kv, int max_pairs) {
 // scales; with kPV8, v holds e4m3 bytes too, dequantised by v_scale.  With a
 // workspace of at least the plan's size the last, partial wave runs split,
 // followed by the combine kernel on the same stream.
-// With kNormQ, q holds un-normalised bf16 queries whose RMS norm (epsilon
-// q_eps) the kernel folds into each row's softmax scale.
-template <bool kQK8, bool kPV8, bool kNormQ = false>
+template <bool kQK8, bool kPV8>
 int launch_pair(const void* q, const void* k, const void* v, void* out, int64_t BH, int Lq, int Lk,
                 double scale, cudaStream_t stream, int max_pairs, void* ws, int64_t ws_bytes,
-                float v_scale = 1.f, float q_eps = 0.f) {
+                float v_scale = 1.f) {
   CUtensorMap tq, tk, tv;
   int rc;
   const int qk_bytes = kQK8 ? 1 : 2;
@@ -927,7 +922,6 @@ int launch_pair(const void* q, const void* k, const void* v, void* out, int64_t 
   p.scale_log2 = static_cast<float>(scale * 1.4426950408889634);
   p.v_scale = v_scale;
   p.inv_v_scale = 1.f / v_scale;
-  p.q_eps = q_eps;
   SplitPlan plan = plan_split(p.num_units, (Lk + dit::kBN - 1) / dit::kBN, max_pairs);
   if (plan.splits > 1 && (!ws || ws_bytes < plan.ws_bytes))
     plan = SplitPlan{p.num_units, 1, p.num_units, 0, 0};
@@ -940,8 +934,7 @@ int launch_pair(const void* q, const void* k, const void* v, void* out, int64_t 
   cudaLaunchAttribute attr;
   cudaLaunchConfig_t cfg =
       pair_launch_config(2 * pairs, stream, &attr, dit::PairTraitsT<kQK8, kPV8>::kSmemBytes);
-  cudaError_t e =
-      cudaLaunchKernelEx(&cfg, dit::fmha_fwd_pair_kernel<kQK8, kPV8, kNormQ>, tq, tk, tv, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, dit::fmha_fwd_pair_kernel<kQK8, kPV8>, tq, tk, tv, p);
   if (e != cudaSuccess) return cuda_fail(e);
   if (plan.splits > 1) {
     const int64_t rows = (plan.num_items - plan.split_base) / plan.splits * int64_t{kPairUnitRows};
@@ -956,10 +949,10 @@ int launch_pair(const void* q, const void* k, const void* v, void* out, int64_t 
 
 // Shared memory and cluster attributes of a pair kernel; *pairs = clusters of
 // two that fit on the device at once.
-template <bool kQK8, bool kPV8, bool kNormQ = false>
+template <bool kQK8, bool kPV8>
 int setup_pair_kernel(int num_sms, int* pairs) {
   const uint32_t smem = dit::PairTraitsT<kQK8, kPV8>::kSmemBytes;
-  auto* kernel = dit::fmha_fwd_pair_kernel<kQK8, kPV8, kNormQ>;
+  auto* kernel = dit::fmha_fwd_pair_kernel<kQK8, kPV8>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return cuda_fail(e);
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
@@ -1063,18 +1056,14 @@ int dit_attn_create(void) {
                            Traits<64>::kSmemBytes);
   if (e != cudaSuccess) return cuda_fail(e);
   {
-    int rc = DIT_ATTN_OK, bf16_pairs = 0, qk8_pairs = 0, fp8_pairs = 0, qnorm_pairs = 0;
+    int rc = DIT_ATTN_OK, bf16_pairs = 0, qk8_pairs = 0, fp8_pairs = 0;
     if ((rc = setup_pair_kernel<false, false>(prop.multiProcessorCount, &bf16_pairs)) != DIT_ATTN_OK)
       return rc;
     if ((rc = setup_pair_kernel<true, false>(prop.multiProcessorCount, &qk8_pairs)) != DIT_ATTN_OK)
       return rc;
     if ((rc = setup_pair_kernel<true, true>(prop.multiProcessorCount, &fp8_pairs)) != DIT_ATTN_OK)
       return rc;
-    if ((rc = setup_pair_kernel<false, false, true>(prop.multiProcessorCount, &qnorm_pairs)) !=
-        DIT_ATTN_OK)
-      return rc;
     g_state[dev].max_pairs = bf16_pairs;
-    g_state[dev].max_pairs_qnorm = qnorm_pairs;
     g_state[dev].max_pairs_qk8 = qk8_pairs;
     g_state[dev].max_pairs_fp8 = fp8_pairs;
   }
@@ -1197,29 +1186,6 @@ int dit_attn_forward_fp8(const void* q8, const void* k8, const void* v8, void* o
                                  v_scale, nullptr, 0, stream);
 }
 
-int dit_attn_forward_qnorm(const void* q, const void* k, const void* v, void* out, int B, int H,
-                           int Lq, int Lk, int d, float scale, float eps, void* workspace,
-                           long long workspace_bytes, void* stream) {
-  int rc = check_forward_args(q, k, v, out, B, H, Lq, Lk, d, scale, 2);
-  if (rc != DIT_ATTN_OK) return rc;
-  if (!std::isfinite(eps) || eps < 0.f) return DIT_ATTN_ERR_INVALID_ARG;
-  if (d != 128) return DIT_ATTN_ERR_UNSUPPORTED;
-  rc = check_workspace(workspace, workspace_bytes, q, k, v, out, B, H, Lq, Lk, d, 2);
-  if (rc != DIT_ATTN_OK) return rc;
-  const int64_t BH = static_cast<int64_t>(B) * H;
-  int dev = -1;
-  if (!current_device(&dev)) return DIT_ATTN_ERR_NO_DEVICE;
-  int max_pairs;
-  {
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_state[dev].ready) return DIT_ATTN_ERR_NOT_INITIALIZED;
-    max_pairs = g_state[dev].max_pairs_qnorm;
-  }
-  return launch_pair<false, false, true>(q, k, v, out, BH, Lq, Lk, scale,
-                                         static_cast<cudaStream_t>(stream), max_pairs, workspace,
-                                         workspace_bytes, 1.f, eps);
-}
-
 }  // extern "C"
 
 extern "C" {
@@ -1251,7 +1217,7 @@ int dit_attn_workspace_size(int B, int H, int Lq, int Lk, int d, int variant, lo
   if (!bytes) return DIT_ATTN_ERR_INVALID_ARG;
   *bytes = 0;
   if (B < 1 || H < 1 || Lq < 1 || Lk < 1) return DIT_ATTN_ERR_INVALID_ARG;
-  if (variant < 0 || variant > 3) return DIT_ATTN_ERR_INVALID_ARG;
+  if (variant < 0 || variant > 2) return DIT_ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return DIT_ATTN_ERR_UNSUPPORTED;
   if (variant != 0 && d != 128) return DIT_ATTN_ERR_UNSUPPORTED;
   const int64_t BH = static_cast<int64_t>(B) * H;
@@ -1265,8 +1231,7 @@ int dit_attn_workspace_size(int B, int H, int Lq, int Lk, int d, int variant, lo
   {
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_state[dev].ready) return DIT_ATTN_ERR_NOT_INITIALIZED;
-    max_pairs = variant == 3   ? g_state[dev].max_pairs_qnorm
-                : variant == 2 ? g_state[dev].max_pairs_fp8
+    max_pairs = variant == 2   ? g_state[dev].max_pairs_fp8
                 : variant == 1 ? g_state[dev].max_pairs_qk8
                                : g_state[dev].max_pairs;
   }

@@ -537,40 +537,12 @@ __device__ __forceinline__ void softmax_tile_lean(uint32_t taddr_s, int key0, bo
   l += sum8(acc);
 }
 
-// Sum of squares of this thread's half of query row r (64 bf16 values, in
-// column order) from a query tile in shared memory: two 128-byte-swizzled
-// boxes of 64 columns, 16-byte unit u of row r at unit u ^ (r mod 8).
-template <class T>
-__device__ __forceinline__ float q_half_row_sum_squares(uint32_t tile, int r, int half) {
-  const uint32_t row = tile + static_cast<uint32_t>(half) * T::kQBoxBytes + r * 128;
-  float ss = 0.f;
-#pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const uint4 v = ld_shared_v4(row + (((u ^ (r & 7))) << 4));
-    const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float lo = __uint_as_float(vv[k] << 16), hi = __uint_as_float(vv[k] & 0xFFFF0000u);
-      ss = fmaf(lo, lo, ss);
-      ss = fmaf(hi, hi, ss);
-    }
-  }
-  return ss;
-}
-
 // Softmax and epilogue of the pair kernel: warp w works on query tile w / 8
 // and, with q = w mod 8, on TMEM lanes (rows) 32*(q%4) + 16*(q/4) .. +15, two
 // threads per row (lanes 0-15 take keys 0-63, lanes 16-31 keys 64-127).
 // Each warp arrives once per key tile on its tile's P-ready barrier of the
 // leader CTA (8 warps x 2 CTAs).
-// With kNormQ the queries arrive un-normalised: at the first key tile of each
-// work item (Q is then in shared memory, since its first product is done),
-// each thread reads its half of its row from the query tile, the two halves'
-// sums of squares are combined, and the row's softmax scale becomes
-// scale_log2 / sqrt(mean(q^2) + eps).  Since qn . k = (q . k) / sqrt(mean(q^2)
-// + eps), this is attention on RMS-normalised queries, without rounding the
-// normalised queries to bf16.
-template <int D, class T, bool kNormQ = false>
+template <int D, class T>
 __device__ void softmax_role_pair(const Params& p, const Shared& sh, uint32_t tmem) {
   const int warp = threadIdx.x / 32;                 // 0..15
   const int lane = threadIdx.x & 31;
@@ -596,26 +568,15 @@ __device__ void softmax_role_pair(const Params& p, const Shared& sh, uint32_t tm
     const WorkItem w = work_item(i, p, n_kv);
     float m_used = -INFINITY;   // running max, in units of s*scale*log2(e)
     float l = 0.f;              // this half-row's share of the row sum
-    float row_scale_log2 = scale_log2;
     for (int j = w.j0; j < w.j1 && ok; ++j, ++g) {
       const bool masked = (j == n_kv - 1) && (tail < kBN);
       const int valid = masked ? tail : kBN;
       const bool got = mbar_wait(sh.bar(T::kBarSFull + t), g & 1u, kWaitLimitNs, sh.abort);
       if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
       tc_fence_after();
-      if constexpr (kNormQ) {
-        if (j == w.j0) {
-          const float ss = q_half_row_sum_squares<T>(sh.base + T::kOffQ + t * T::kQTileBytes, r,
-                                                     half);
-          const float mean = (ss + __shfl_xor_sync(0xffffffffu, ss, 16)) * (1.f / D);
-          // an all-zero row (query rows past Lq) with eps = 0 has no norm: weigh its keys alike
-          const float inv = (mean > 0.f || p.q_eps > 0.f) ? rsqrtf(mean + p.q_eps) : 0.f;
-          row_scale_log2 = scale_log2 * inv;
-        }
-      }
       // O_t is quiescent here: S_t's completion implies the previous P.V
       // product into O_t finished.
-      softmax_tile_lean<D, T::kP8>(taddr_s, key0, j == w.j0, masked, valid, row_scale_log2, m_used,
+      softmax_tile_lean<D, T::kP8>(taddr_s, key0, j == w.j0, masked, valid, scale_log2, m_used,
                                    l, [&](float f) { rescale_o_half<D>(taddr_o, f); });
       tmem_wait_st();
       tc_fence_before();
@@ -662,15 +623,12 @@ __device__ void softmax_role_pair(const Params& p, const Shared& sh, uint32_t tm
 
 // ----------------------------------------------------------------- kernel
 // Launched with a cluster dimension of 2 (consecutive CTAs form a pair).
-// kNormQ (bf16 only): queries arrive un-normalised; their RMS norm is folded
-// into each row's softmax scale (softmax_role_pair).
-template <bool kQK8, bool kPV8, bool kNormQ = false>
+template <bool kQK8, bool kPV8>
 __global__ void __launch_bounds__(kPairThreads, 1)
     fmha_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ,
                          const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const Params p) {
   using T = PairTraitsT<kQK8, kPV8>;
-  static_assert(!(kNormQ && kQK8), "the fused query normalisation is a bf16-query variant");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -720,7 +678,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 
   if (warp < kPairMmaWarp) {
     reg_alloc<kPairRegsSoftmax>();
-    softmax_role_pair<T::D, T, kNormQ>(p, sh, tmem);
+    softmax_role_pair<T::D, T>(p, sh, tmem);
     if (leader && threadIdx.x == 0 && *sh.abort) pair_teardown_drain<T>(sh);
   } else if (warp == kPairMmaWarp) {
     reg_dealloc<kPairRegsOther>();

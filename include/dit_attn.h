@@ -128,8 +128,7 @@ int dit_attn_forward_noalloc(const void* q, const void* k, const void* v, void* 
 
 /*
  * Workspace bytes that dit_attn_forward_ws (variant 0), dit_attn_forward_qk8_ws
- * (variant 1), dit_attn_forward_fp8_ws (variant 2) or dit_attn_forward_qnorm
- * (variant 3) uses for these sizes on
+ * (variant 1) or dit_attn_forward_fp8_ws (variant 2) uses for these sizes on
  * the current device; 0 when no split applies (d = 64, or the last wave is
  * full or its units too short).  Another variant is INVALID_ARG.  Size
  * arguments as for the forward calls; requires dit_attn_create().
@@ -203,34 +202,6 @@ int dit_attn_forward_fp8_ws(const void* q8, const void* k8, const void* v8, void
                             int H, int Lq, int Lk, int d, float scale, float q_scale,
                             float k_scale, float v_scale, void* workspace,
                             long long workspace_bytes, void* stream);
-
-/*
- * dit_attn_forward_ws on queries that are not yet RMS-normalised (the
- * 1024x1024 and 2048x2048 workloads normalise Q and K per token and head
- * before attention; the pages do not print the norm, and no learned weight
- * is read):
- *
- *     qn[b,h,i,:] = q[b,h,i,:] / sqrt(mean_c q[b,h,i,c]^2 + eps)
- *     out = softmax(qn k^T * scale) v
- *
- * The norm is folded into each query row's softmax scale (qn . k equals
- * q . k / sqrt(mean(q^2) + eps)): at the start of every work item the
- * softmax threads read their row from the query tile already in shared
- * memory, in fp32, and multiply the row's logit scale by the reciprocal
- * root.  No separate pass over Q and no bf16 rounding of the normalised
- * queries (so the result differs from dit_attn_rmsnorm + dit_attn_forward_ws
- * by that rounding, within the forward's tolerance).  Keys are re-read for
- * every query block, so they stay on the dit_attn_rmsnorm prologue.
- *   q: device bf16 [B, H, Lq, d], un-normalised; k: as the caller wants it
- *   (normally through dit_attn_rmsnorm); v, out, workspace as in
- *   dit_attn_forward_ws.  eps finite and >= 0 (else INVALID_ARG); a query row
- *   of zeros with eps = 0 has no norm and weighs its keys alike.  d must be
- *   128 (else UNSUPPORTED).  Workspace sizes: dit_attn_workspace_size
- *   variant 3.  Otherwise as dit_attn_forward_ws.
- */
-int dit_attn_forward_qnorm(const void* q, const void* k, const void* v, void* out, int B, int H,
-                           int Lq, int Lk, int d, float scale, float eps, void* workspace,
-                           long long workspace_bytes, void* stream);
 
 /*
  * Per-tensor e4m3 quantisation (the prologue that gives dit_attn_forward_fp8

@@ -339,35 +339,3 @@ def test_check_exp2_validates_before_cuda():
     assert lib.dit_attn_check_exp2(A, A + MB, A + 2 * MB, 8, 4, None) == 1         # degree 4
     assert lib.dit_attn_check_exp2(A + 2, A + MB, A + 2 * MB, 8, 3, None) == 1     # misaligned
     assert lib.dit_attn_check_exp2(A, A + 16, A + 2 * MB, 8, 3, None) == 1         # overlap
-
-
-# ----------------------------------------------------------------- forward with the fused query norm
-
-QN = (A, A + MB, A + 2 * MB, A + 3 * MB, 1, 1, 8, 8, 128, 0.125, 1e-6, 0, 0)
-
-
-def _qn(**change):
-    names = ("q", "k", "v", "out", "B", "H", "Lq", "Lk", "d", "scale", "eps", "workspace",
-             "workspace_bytes")
-    args = dict(zip(names, QN))
-    args.update(change)
-    return tuple(args[n] for n in names)
-
-
-@pytest.mark.parametrize("args,expect", [
-    (_qn(q=0), 1),                                    # null q
-    (_qn(eps=-1.0), 1),                               # negative eps
-    (_qn(eps=float("nan")), 1),
-    (_qn(scale=float("inf")), 1),
-    (_qn(workspace=A + 4 * MB + 8, workspace_bytes=4096), 1),   # misaligned workspace
-    (_qn(d=64), 2),                                   # d = 128 only
-    (_qn(B=65536, H=65536), 2),
-])
-def test_forward_qnorm_rejects_bad_arguments(args, expect):
-    assert dit.forward_qnorm_ptr(*args) == expect
-
-
-@pytest.mark.skipif(_has_gpu(), reason="a valid call with fake pointers must not reach a GPU")
-def test_forward_qnorm_no_device():
-    assert dit.forward_qnorm_ptr(*QN) == 4
-    assert dit.forward_qnorm_ptr(*_qn(eps=0.0, scale=-0.3)) == 4

@@ -240,3 +240,33 @@ def test_graph_replay_split_tail(dit):
     torch.cuda.synchronize()
     assert_close(to_host_f64(out), oracle_full(qh, kh, vh, 0.088), "split tail graph replay")
     assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+
+
+def test_graph_replay_rmsnorm_prologue_pipeline(dit):
+    """The RMS-norm prologue pipeline captured as one graph (dit_attn_rmsnorm of
+    raw Q and of raw K, then the forward): the replay meets the bf16 bar
+    against the oracle's RMS norm + attention and equals the eager calls."""
+    import torch
+    rng = np.random.default_rng(25)
+    B, H, Lq, Lk, d = 1, 3, 1100, 1300, 128
+    qh = W.random_bf16(rng, (B, H, Lq, d), 2.0)
+    kh = W.random_bf16(rng, (B, H, Lk, d), 0.5)
+    vh = W.random_bf16(rng, (B, H, Lk, d))
+    q, k, v = to_device(qh), to_device(kh), to_device(vh)
+    scale = float(np.float32(1 / math.sqrt(d)))
+
+    def pipeline(qn, kn, out):
+        dit.rmsnorm(q, out=qn)
+        dit.rmsnorm(k, out=kn)
+        dit.forward(qn, kn, v, scale, out=out)
+
+    eager = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(q))
+    pipeline(*eager)
+    captured = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(q))
+    g = _capture(lambda: pipeline(*captured))
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(captured[2].view(torch.int16), eager[2].view(torch.int16))
+    want = oracle.attention(oracle.rmsnorm(qh, None, 1e-6), oracle.rmsnorm(kh, None, 1e-6),
+                            W.bf16_to_f32(vh).astype(np.float64), scale)
+    assert_close(to_host_f64(captured[2]), want, "RMS-norm pipeline graph replay")
