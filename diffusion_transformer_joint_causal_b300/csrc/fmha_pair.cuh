@@ -53,10 +53,6 @@ constexpr int kPairLoadWarp = 17;
 constexpr int kPairRegsSoftmax = 112;
 constexpr int kPairRegsOther = 32;
 
-// One MMA issuer per query tile (pair_mma_role_tile) instead of one for both.
-constexpr bool kTwoIssuers = true;
-constexpr int kPairMmaWarp1 = 18;   // issuer of query tile 1 (leader CTA)
-
 // e4m3 probabilities: p = 2^(x - m + kProbOffsetE4M3) with the lazy rescale at
 // kRescaleThresholdE4M3, so p <= 2^8 after a max pass; an optimistic pass is
 // kept while its rounded row sum stays below 448 (no value saturated).  With
@@ -378,95 +374,6 @@ __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) 
   __syncwarp();
 }
 
-// Per-tile MMA issuer (kTwoIssuers): the leader's warp 16 issues every MMA of
-// query tile 0 and warp 18 every MMA of tile 1.  A tcgen05.mma issue blocks
-// until the tensor pipe takes the instruction (the queue is shallow), so a
-// single issuer that waits for P-ready or a full stage leaves the pipe idle;
-// with one issuer per tile one issues while the other waits.  Both walk the
-// same ring of K/V stages; a stage is released when both have committed the
-// products that read it (the empty barriers count two arrivals).  Per tile
-// the order is the single issuer's: S_t = Q_t K_0^T, then per key tile j
-// O_t += P_t V_j and S_t = Q_t K_(j+1)^T, so P_t (aliased over S_t) is always
-// read before it is overwritten.
-template <bool kQK8, bool kPV8, int t>
-__device__ void pair_mma_role_tile(const Params& p, const Shared& sh, uint32_t tmem) {
-  using T = PairTraitsT<kQK8, kPV8>;
-  constexpr uint16_t kBoth = 3;
-  const bool issuer = (threadIdx.x & 31) == 0;
-  uint32_t stage = 0, phase = 0, g = 0, it = 0;
-  bool ok = true;
-  const int n_kv = (p.Lk + kBN - 1) / kBN;
-  const uint32_t q_lo = desc_lo_sw128(sh.base + T::kOffQ + t * T::kQTileBytes, 16);
-  const uint32_t kv_lo0 = desc_lo_sw128(sh.base + T::kOffKV, 16);
-  const uint32_t d_s = tmem + T::col_s(t), d_o = tmem + T::col_o(t);
-  auto kv_lo = [&](uint32_t s) { return kv_lo0 + s * (T::kHalfBytes >> 4); };
-  auto wait = [&](int bar, uint32_t parity) -> bool {
-    const bool got = mbar_wait(sh.bar(bar), parity, kWaitLimitNs, sh.abort);
-    return __all_sync(0xffffffffu, got);
-  };
-  auto take_stage = [&](uint32_t& s_out) -> bool {
-    s_out = stage;
-    if (!wait(T::kBarFull + stage, phase)) return false;
-    if (++stage == T::kStages) { stage = 0; phase ^= 1u; }
-    return true;
-  };
-
-  for (int i = static_cast<int>(cluster_id_x()); i < p.num_items && ok;
-       i += static_cast<int>(num_clusters_x()), ++it) {
-    int n = n_kv;                // key tiles of this item
-    if (i >= p.split_base) {
-      const int sp = (i - p.split_base) % p.splits;
-      n = (sp + 1) * n_kv / p.splits - sp * n_kv / p.splits;
-    }
-    uint32_t sK = 0, sV = 0, sK_next = 0, sV_next = 0;
-    ok = wait(T::kBarQFull + t, it & 1u) && take_stage(sK);
-    if (!ok) break;
-    tc_fence_after();
-    if (issuer) {
-      pair_issue_qk<kQK8>(d_s, q_lo, kv_lo(sK));
-      mma_commit_pair(sh.bar(T::kBarSFull + t), kBoth);
-      if (n == 1) mma_commit_pair(sh.bar(T::kBarQEmpty + t), kBoth);
-      mma_commit_pair(sh.bar(T::kBarEmpty + sK), kBoth);
-    }
-    __syncwarp();
-    ok = take_stage(sV) && (n == 1 || take_stage(sK_next));
-    if (!ok) break;
-
-    for (int j = 0; j < n && ok; ++j, ++g) {
-      // held: sV = V(j); sK_next = K(j+1) when j+1 < n
-      const bool more = j + 1 < n;
-      ok = wait(T::kBarPFull + t, g & 1u);
-      if (!ok) break;
-      tc_fence_after();
-      if (issuer) {
-        pair_issue_pv<kPV8>(d_o, d_s, kv_lo(sV), j > 0);
-        if (more) {
-          pair_issue_qk<kQK8>(d_s, q_lo, kv_lo(sK_next));
-          mma_commit_pair(sh.bar(T::kBarSFull + t), kBoth);
-          if (j + 2 == n) mma_commit_pair(sh.bar(T::kBarQEmpty + t), kBoth);
-          mma_commit_pair(sh.bar(T::kBarEmpty + sV), kBoth);
-          mma_commit_pair(sh.bar(T::kBarEmpty + sK_next), kBoth);
-        } else {
-          mma_commit_pair(sh.bar(T::kBarEmpty + sV), kBoth);
-          mma_commit_pair(sh.bar(T::kBarOFull + t), kBoth);
-        }
-      }
-      __syncwarp();
-      if (more) ok = take_stage(sV_next) && (j + 2 >= n || take_stage(sK));
-      sV = sV_next;
-      sK_next = sK;   // K(j+2), taken above when it exists
-    }
-  }
-  if (!ok && issuer) record_timeout<true>(sh);
-  if (issuer) {
-    // the drain barrier counts both issuers' commits
-    mma_commit_pair(sh.bar(T::kBarDrain), 1);
-    const volatile int no_abort = 0;
-    mbar_wait(sh.bar(T::kBarDrain), 0, kWaitLimitNs, &no_abort);
-  }
-  __syncwarp();
-}
-
 // ----------------------------------------------------------------- softmax (pair kernel)
 // Largest scaled logit s * scale_log2 of 32 logits, keys at or beyond `valid`
 // excluded (-inf when all are).  Scaling is monotone, so this is scale_log2
@@ -739,7 +646,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < T::kStages; ++s) {
       mbar_init(sh.bar(T::kBarFull + s), 1);
-      mbar_init(sh.bar(T::kBarEmpty + s), kTwoIssuers ? 2 : 1);
+      mbar_init(sh.bar(T::kBarEmpty + s), 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(sh.bar(T::kBarQFull + t), 1);
@@ -748,7 +655,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
       mbar_init(sh.bar(T::kBarPFull + t), T::kPFullArrivals);
       mbar_init(sh.bar(T::kBarOFull + t), 1);
     }
-    mbar_init(sh.bar(T::kBarDrain), kTwoIssuers ? 2 : 1);
+    mbar_init(sh.bar(T::kBarDrain), 1);
     mbar_init(sh.bar(T::kBarProdDone), 2);
     *sh.abort = 0;
     fence_mbarrier_init();
@@ -775,17 +682,13 @@ __global__ void __launch_bounds__(kPairThreads, 1)
     if (leader && threadIdx.x == 0 && *sh.abort) pair_teardown_drain<T>(sh);
   } else if (warp == kPairMmaWarp) {
     reg_dealloc<kPairRegsOther>();
-    if (leader) {
-      if constexpr (kTwoIssuers) pair_mma_role_tile<kQK8, kPV8, 0>(p, sh, tmem);
-      else pair_mma_role<kQK8, kPV8>(p, sh, tmem);
-    }
+    if (leader) pair_mma_role<kQK8, kPV8>(p, sh, tmem);
   } else if (warp == kPairLoadWarp) {
     reg_dealloc<kPairRegsOther>();
     if (lane == 0) pair_load_role<kQK8, kPV8>(&tmQ, &tmK, &tmV, p, sh);
     __syncwarp();
   } else {
     reg_dealloc<kPairRegsOther>();
-    if (kTwoIssuers && warp == kPairMmaWarp1 && leader) pair_mma_role_tile<kQK8, kPV8, 1>(p, sh, tmem);
   }
 
   // The leader drained its MMAs and, after a give-up, every copy either CTA
