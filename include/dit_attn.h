@@ -29,8 +29,9 @@
  *
  * Streams: work is enqueued on `stream` (a cudaStream_t; NULL = the legacy
  * default stream).  No call synchronises, except dit_attn_get_device_error.
- * Calls keep no per-call device state, so calls on different streams may
- * overlap.
+ * The forward calls keep no per-call device state of their own (the split
+ * tail's workspace belongs to the caller), so calls on different streams may
+ * overlap; dit_attn_forward_noalloc is the exception (its scratch is shared).
  *
  * Errors: every entry point returns a dit_attn_status.  Argument checks run
  * before any CUDA call, so an invalid call has no side effect.
@@ -106,10 +107,11 @@ int dit_attn_forward_ws(const void* q, const void* k, const void* v, void* out, 
  * forbids later allocations, code running inside a memory allocator's own
  * callback, or a latency-bound loop that must not enter cudaMalloc (which can
  * synchronise the device).  The pages have no counterpart of this entry
- * point; it exists for embedding.  The split tail's scratch is a file-scope device array of
- * the library, 80 key-range chunks of 512 x 130 fp32 (21.3 MB), resident on
- * every device from when the library's device code is loaded there (at the
- * latest, its first kernel launch or dit_attn_create) until the process exits.
+ * point; it exists for embedding.  The split tail's scratch is a file-scope
+ * device array of the library, 80 key-range chunks of 512 x 130 fp32
+ * (21.3 MB), resident on every device from when the library's device code is
+ * loaded there (at the latest, its first kernel launch or dit_attn_create)
+ * until the process exits.
  * dit_attn_create() takes the array's device address for the current device;
  * the call itself allocates nothing (no cudaMalloc, no library allocator) and
  * takes no workspace argument.
