@@ -91,7 +91,8 @@ constexpr int kMiscFills = 2;
 constexpr int kMiscQLoads = 3;
 constexpr int kMiscPeerFills = 5;
 constexpr int kMiscPeerQLoads = 6;
-constexpr int kMiscWords = 8;
+constexpr int kMiscSlotBytes = 8;   // [8, 8 + ring slots): this CTA's bytes of each slot's last fill
+constexpr int kMiscWords = 24;
 
 template <int D>
 struct Traits {

@@ -75,16 +75,20 @@ struct PairTraitsT {
   static constexpr uint32_t kKBoxBytes = 64u * 128u;        // 64 keys x 128 bytes
   static constexpr uint32_t kKHalfBytes = kQKBoxes * kKBoxBytes;   // one K half
   static constexpr uint32_t kVHalfBytes = kPV8 ? 128u * 64u : 128u * 128u;  // 128 keys x 64 columns
-  static constexpr uint32_t kHalfBytes = kPV8 ? 8192 : 16384;  // a stage: one V half (or K half)
-  static constexpr int kStages = kPV8 ? 20 : (kQK8 ? 10 : 8);
+  // A ring slot holds what one key-tile iteration of the MMA warp reads:
+  // V(j) for P.V and K(j+1) for the next Q K^T (the first slot of a work
+  // item holds K(0) alone, its last slot V(n-1) alone).  K at offset 0, V
+  // after it.
+  static constexpr uint32_t kSlotBytes = kKHalfBytes + kVHalfBytes;
+  static constexpr int kStages = kPV8 ? 10 : (kQK8 ? 6 : 4);   // ring slots
   __host__ __device__ static constexpr uint32_t col_s(int t) { return 128u * t; }
   __host__ __device__ static constexpr uint32_t col_o(int t) { return 256u + 128u * t; }
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffKV = 2 * kQTileBytes;
-  static constexpr uint32_t kOffBar = kOffKV + kStages * kHalfBytes;
-  static constexpr int kBarFull = 0;                 // leader: both halves of a stage landed
-  static constexpr int kBarEmpty = kStages;          // both: the stage may be refilled
+  static constexpr uint32_t kOffBar = kOffKV + kStages * kSlotBytes;
+  static constexpr int kBarFull = 0;                 // leader: both CTAs' copies of a slot landed
+  static constexpr int kBarEmpty = kStages;          // both: the slot may be refilled
   static constexpr int kBarQFull = 2 * kStages;      // leader: both CTAs' query tile t landed
   static constexpr int kBarQEmpty = kBarQFull + 2;   // both
   static constexpr int kBarSFull = kBarQEmpty + 2;   // both
@@ -110,8 +114,9 @@ __device__ void pair_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
   const uint64_t pol_q = policy_evict_first();
   const uint32_t full0_leader = mapa_shared(sh.bar(T::kBarFull), 0);
   const uint32_t qfull0_leader = mapa_shared(sh.bar(T::kBarQFull), 0);
-  // fills: K/V half-stage copies issued so far (stage = fills mod kStages);
-  // q_loads0/1: query-tile-0/1 copies issued so far.  Both are left in shared
+  // fills: slot fills issued so far (slot = fills mod kStages); each fill's
+  // byte count (this CTA's share) is kept per slot in the misc words;
+  // q_loads0/1: query-tile-0/1 copies issued so far.  All are left in shared
   // memory for the teardown drain.
   uint32_t stage = 0, phase = 0, fills = 0, it = 0, q_loads0 = 0, q_loads1 = 0;
   bool ok = true;
@@ -128,10 +133,21 @@ __device__ void pair_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
     else ++q_loads1;
     return true;
   };
-  auto take_empty = [&](uint32_t half_bytes) -> bool {
+  auto take_empty = [&](uint32_t bytes) -> bool {   // bytes: this CTA's copies into the slot
     if (!mbar_wait(sh.bar(T::kBarEmpty + stage), phase ^ 1u, kWaitLimitNs, sh.abort)) return false;
-    if (leader) mbar_arrive_expect_tx(sh.bar(T::kBarFull + stage), 2 * half_bytes);
+    if (leader) mbar_arrive_expect_tx(sh.bar(T::kBarFull + stage), 2 * bytes);
+    st_shared_u32(sh.misc_word(kMiscSlotBytes + static_cast<int>(stage)), bytes);
     return true;
+  };
+  auto slot_base = [&]() { return sh.base + T::kOffKV + stage * T::kSlotBytes; };
+  auto load_k = [&](int j, int bh) {   // keys j*128 + 64*rank .. +63, all d columns
+    for (int b = 0; b < T::kQKBoxes; ++b)
+      tma_load_3d_pair(slot_base() + b * T::kKBoxBytes, tmK, full0_leader + 8u * stage,
+                       b * T::kBoxCols, j * kBN + static_cast<int>(rank) * 64, bh, pol_kv);
+  };
+  auto load_v = [&](int j, int bh) {   // keys j*128 .. +127, columns 64*rank .. +63
+    tma_load_3d_pair(slot_base() + T::kKHalfBytes, tmV, full0_leader + 8u * stage,
+                     static_cast<int>(rank) * 64, j * kBN, bh, pol_kv);
   };
   auto advance = [&]() {
     ++fills;
@@ -143,27 +159,17 @@ __device__ void pair_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
     const WorkItem w = work_item(i, p, n_kv);
     const int bh = w.bh;
     const int row0 = w.qblock * (2 * kUnitRows) + static_cast<int>(rank) * kUnitRows;
-    ok = load_q(0, bh, row0);
+    ok = load_q(0, bh, row0) && take_empty(T::kKHalfBytes);
+    if (!ok) break;
+    load_k(w.j0, bh);   // the item's first slot: K(j0)
+    advance();
+    ok = load_q(1, bh, row0);
     for (int j = w.j0; j < w.j1 && ok; ++j) {
-      // K half: keys j*128 + 64*rank .. +63, all d columns (128-byte boxes)
-      ok = take_empty(T::kKHalfBytes);
+      const bool more = j + 1 < w.j1;
+      ok = take_empty(T::kVHalfBytes + (more ? T::kKHalfBytes : 0u));
       if (!ok) break;
-      {
-        const uint32_t dst = sh.base + T::kOffKV + stage * T::kHalfBytes;
-        for (int b = 0; b < T::kQKBoxes; ++b)
-          tma_load_3d_pair(dst + b * T::kKBoxBytes, tmK, full0_leader + 8u * stage, b * T::kBoxCols,
-                           j * kBN + static_cast<int>(rank) * 64, bh, pol_kv);
-      }
-      advance();
-      if (j == w.j0) {
-        ok = load_q(1, bh, row0);
-        if (!ok) break;
-      }
-      // V half: keys j*128 .. +127, columns 64*rank .. +63
-      ok = take_empty(T::kVHalfBytes);
-      if (!ok) break;
-      tma_load_3d_pair(sh.base + T::kOffKV + stage * T::kHalfBytes, tmV, full0_leader + 8u * stage,
-                       static_cast<int>(rank) * 64, j * kBN, bh, pol_kv);
+      load_v(j, bh);
+      if (more) load_k(j + 1, bh);
       advance();
     }
   }
@@ -187,12 +193,12 @@ __device__ void pair_load_role(const CUtensorMap* tmQ, const CUtensorMap* tmK,
 // the CTAs' shared memory goes away.  Both producers report how many copies
 // they issued and arrive on the leader's producer-done barrier.  All copies
 // complete on the leader's barriers, and a barrier phase only completes when
-// the leader armed it for both halves and both halves landed, but the two
+// the leader armed it for both CTAs' shares and both landed, but the two
 // producers may have stopped at different points.  For each of the last
-// kStages K/V fills and each query tile's last load, the leader balances the
-// phase: where only the leader issued the fill it retires the missing half's
-// bytes itself (mbarrier.complete_tx), where only the peer did it arms the
-// phase for that half alone; then it waits (bounded) for the phase.
+// kStages slot fills and each query tile's last load, the leader balances the
+// phase: where only the leader issued the fill it retires the peer's share of
+// the bytes itself (mbarrier.complete_tx), where only the peer did it arms the
+// phase for the peer's share alone; then it waits (bounded) for the phase.
 template <class T>
 __device__ void pair_teardown_drain(const Shared& sh) {
   const volatile int no_abort = 0;
@@ -205,15 +211,19 @@ __device__ void pair_teardown_drain(const Shared& sh) {
     mbar_wait(bar, parity, kWaitLimitNs, &no_abort);
   };
   // fill counts of the two producers differ by at most kStages (each waits
-  // for the consumption of the fill kStages back, which needs both halves)
+  // for the consumption of the fill kStages back, which needs both halves);
+  // each CTA keeps its share of every slot's bytes, the peer's read remotely
   const uint32_t fl = word(kMiscFills), fp = word(kMiscPeerFills);
   const uint32_t last = static_cast<int32_t>(fp - fl) > 0 ? fp : fl;
   const uint32_t window = last < static_cast<uint32_t>(T::kStages) ? last : T::kStages;
   for (uint32_t k = 1; k <= window; ++k) {
-    const uint32_t f = last - k;   // fills alternate K half (even f), V half (odd f)
-    balance_and_wait(sh.bar(T::kBarFull + static_cast<int>(f % T::kStages)),
-                     static_cast<int32_t>(f - fl) < 0, static_cast<int32_t>(f - fp) < 0,
-                     (f & 1u) ? T::kVHalfBytes : T::kKHalfBytes, (f / T::kStages) & 1u);
+    const uint32_t f = last - k;
+    const int slot = static_cast<int>(f % T::kStages);
+    const bool by_leader = static_cast<int32_t>(f - fl) < 0, by_peer = static_cast<int32_t>(f - fp) < 0;
+    const uint32_t bytes =
+        by_leader ? word(kMiscSlotBytes + slot)
+                  : ld_shared_cluster_u32(mapa_shared(sh.misc_word(kMiscSlotBytes + slot), 1u));
+    balance_and_wait(sh.bar(T::kBarFull + slot), by_leader, by_peer, bytes, (f / T::kStages) & 1u);
   }
   // query tiles: the two producers' load counts differ by at most one
   for (int t = 0; t < 2; ++t) {
@@ -281,23 +291,23 @@ __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) 
   const uint32_t q_lo0 = desc_lo_sw128(sh.base + T::kOffQ, 16);
   const uint32_t q_lo1 = desc_lo_sw128(sh.base + T::kOffQ + T::kQTileBytes, 16);
   const uint32_t kv_lo0 = desc_lo_sw128(sh.base + T::kOffKV, 16);
-  auto kv_lo = [&](uint32_t s) { return kv_lo0 + s * (T::kHalfBytes >> 4); };
+  auto k_lo = [&](uint32_t s) { return kv_lo0 + s * (T::kSlotBytes >> 4); };
+  auto v_lo = [&](uint32_t s) { return k_lo(s) + (T::kKHalfBytes >> 4); };
   auto wait = [&](int bar, uint32_t parity) -> bool {
     const bool got = mbar_wait(sh.bar(bar), parity, kWaitLimitNs, sh.abort);
     return __all_sync(0xffffffffu, got);
   };
-  auto take_stage = [&](uint32_t& s_out) -> bool {
+  auto take_slot = [&](uint32_t& s_out) -> bool {
     s_out = stage;
     if (!wait(T::kBarFull + stage, phase)) return false;
     if (++stage == T::kStages) { stage = 0; phase ^= 1u; }
     return true;
   };
-  auto wait_q = [&](int t) -> bool { return wait(T::kBarQFull + t, it & 1u); };
 
-  // Stage waits for the next key tile (its V and the following K) happen while
-  // the warp waits for P_1 anyway, off the path from P-ready to the next MMA.
-  // Commits follow the MMA block they track (a commit between MMAs stalls
-  // the issuing thread).
+  // One slot per key tile: iteration j reads V(j) and K(j+1) from the slot
+  // taken while the warp would wait for P_1 of the iteration before, and
+  // releases it with one commit.  Commits follow the MMA block they track (a
+  // commit between MMAs stalls the issuing thread).
   for (int i = static_cast<int>(cluster_id_x()); i < p.num_items && ok;
        i += static_cast<int>(num_clusters_x()), ++it) {
     int n = n_kv;                // key tiles of this item
@@ -305,37 +315,37 @@ __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) 
       const int s = (i - p.split_base) % p.splits;
       n = (s + 1) * n_kv / p.splits - s * n_kv / p.splits;
     }
-    uint32_t sK = 0, sV = 0, sK_next = 0, sV_next = 0;
-    ok = wait_q(0) && take_stage(sK);
+    uint32_t s0 = 0, sCur = 0, sNext = 0;
+    ok = wait(T::kBarQFull + 0, it & 1u) && take_slot(s0);   // K(0)
     if (!ok) break;
     tc_fence_after();
     if (issuer) {
-      pair_issue_qk<kQK8>(tmem + T::col_s(0), q_lo0, kv_lo(sK));
+      pair_issue_qk<kQK8>(tmem + T::col_s(0), q_lo0, k_lo(s0));
       mma_commit_pair(sh.bar(T::kBarSFull + 0), kBoth);
       if (n == 1) mma_commit_pair(sh.bar(T::kBarQEmpty + 0), kBoth);
     }
     __syncwarp();
-    ok = wait_q(1) && take_stage(sV) && (n == 1 || take_stage(sK_next));
+    ok = wait(T::kBarQFull + 1, it & 1u) && take_slot(sCur);   // V(0), K(1)
     if (!ok) break;
     tc_fence_after();
     if (issuer) {
-      pair_issue_qk<kQK8>(tmem + T::col_s(1), q_lo1, kv_lo(sK));
+      pair_issue_qk<kQK8>(tmem + T::col_s(1), q_lo1, k_lo(s0));
       mma_commit_pair(sh.bar(T::kBarSFull + 1), kBoth);
       if (n == 1) mma_commit_pair(sh.bar(T::kBarQEmpty + 1), kBoth);
-      mma_commit_pair(sh.bar(T::kBarEmpty + sK), kBoth);
+      mma_commit_pair(sh.bar(T::kBarEmpty + s0), kBoth);
     }
     __syncwarp();
 
     for (int j = 0; j < n && ok; ++j, ++g) {   // j: tile index within the item
-      // held: sV = V(j); sK_next = K(j+1) when j+1 < n
+      // held: sCur = V(j) (and K(j+1) when j+1 < n)
       const bool more = j + 1 < n;
       ok = wait(T::kBarPFull + 0, g & 1u);
       if (!ok) break;
       tc_fence_after();
       if (issuer) {
-        pair_issue_pv<kPV8>(tmem + T::col_o(0), tmem + T::col_s(0), kv_lo(sV), j > 0);
+        pair_issue_pv<kPV8>(tmem + T::col_o(0), tmem + T::col_s(0), v_lo(sCur), j > 0);
         if (more) {
-          pair_issue_qk<kQK8>(tmem + T::col_s(0), q_lo0, kv_lo(sK_next));
+          pair_issue_qk<kQK8>(tmem + T::col_s(0), q_lo0, k_lo(sCur));
           mma_commit_pair(sh.bar(T::kBarSFull + 0), kBoth);
           if (j + 2 == n) mma_commit_pair(sh.bar(T::kBarQEmpty + 0), kBoth);
         } else {
@@ -343,26 +353,24 @@ __device__ void pair_mma_role(const Params& p, const Shared& sh, uint32_t tmem) 
         }
       }
       __syncwarp();
-      if (more) ok = take_stage(sV_next) && (j + 2 >= n || take_stage(sK));
+      if (more) ok = take_slot(sNext);   // V(j+1), K(j+2)
       ok = ok && wait(T::kBarPFull + 1, g & 1u);
       if (!ok) break;
       tc_fence_after();
       if (issuer) {
-        pair_issue_pv<kPV8>(tmem + T::col_o(1), tmem + T::col_s(1), kv_lo(sV), j > 0);
+        pair_issue_pv<kPV8>(tmem + T::col_o(1), tmem + T::col_s(1), v_lo(sCur), j > 0);
         if (more) {
-          pair_issue_qk<kQK8>(tmem + T::col_s(1), q_lo1, kv_lo(sK_next));
-          mma_commit_pair(sh.bar(T::kBarEmpty + sV), kBoth);
+          pair_issue_qk<kQK8>(tmem + T::col_s(1), q_lo1, k_lo(sCur));
           mma_commit_pair(sh.bar(T::kBarSFull + 1), kBoth);
           if (j + 2 == n) mma_commit_pair(sh.bar(T::kBarQEmpty + 1), kBoth);
-          mma_commit_pair(sh.bar(T::kBarEmpty + sK_next), kBoth);
+          mma_commit_pair(sh.bar(T::kBarEmpty + sCur), kBoth);
         } else {
-          mma_commit_pair(sh.bar(T::kBarEmpty + sV), kBoth);
+          mma_commit_pair(sh.bar(T::kBarEmpty + sCur), kBoth);
           mma_commit_pair(sh.bar(T::kBarOFull + 1), kBoth);
         }
       }
       __syncwarp();
-      sV = sV_next;
-      sK_next = sK;   // K(j+2), taken above when it exists
+      sCur = sNext;
     }
   }
   if (!ok && issuer) record_timeout<true>(sh);
