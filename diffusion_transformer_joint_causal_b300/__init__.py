@@ -331,8 +331,9 @@ def rmsnorm(x, weight=None, eps: float = 1e-6, out=None, stream=None):
         raise ValueError("weight must be a contiguous bf16 [d] tensor on x's device")
     if out is None:
         out = torch.empty_like(x)
-    elif out.dtype != torch.bfloat16 or out.shape != x.shape or not out.is_contiguous():
-        raise ValueError("out must be a contiguous bf16 tensor shaped like x")
+    elif (out.dtype != torch.bfloat16 or out.shape != x.shape or not out.is_contiguous()
+          or out.device != x.device):
+        raise ValueError("out must be a contiguous bf16 tensor shaped like x on x's device")
     with torch.cuda.device(x.device):
         rc = rmsnorm_ptr(x.data_ptr(), out.data_ptr(), weight.data_ptr() if weight is not None else 0,
                          x.numel() // d, d, float(eps), _stream_handle(stream))

@@ -84,3 +84,24 @@ def test_rmsnorm_then_attention_matches_normalised_workload(dit):
     ref = oracle.attention(bits(qn).reshape(q.shape), bits(kn).reshape(k.shape), v,
                            float(np.float32(0.08838834764831845)))
     assert_close(to_host_f64(out), ref, "rmsnorm + attention")
+
+
+def test_host_output_tensors_are_refused_before_any_launch(dit):
+    """An output tensor in host memory would reach a kernel as a host pointer;
+    every binding that takes ``out`` refuses it (and a wrong dtype) with
+    ValueError, and nothing is launched."""
+    import torch
+    x = torch.randn(64, 128, device="cuda").to(torch.bfloat16)
+    with pytest.raises(ValueError):
+        dit.rmsnorm(x, out=torch.empty(64, 128, dtype=torch.bfloat16))
+    with pytest.raises(ValueError):
+        dit.rmsnorm(x, out=torch.empty(64, 128, dtype=torch.float16, device="cuda"))
+    with pytest.raises(ValueError):
+        dit.rmsnorm_e4m3(x, 1.0, out=torch.empty(64, 128, dtype=torch.uint8))
+    with pytest.raises(ValueError):
+        dit.quantize_e4m3(x, 1.0, out=torch.empty(64, 128, dtype=torch.uint8))
+    q = x.view(1, 1, 64, 128)
+    with pytest.raises(ValueError):
+        dit.forward(q, q, q, out=torch.empty(1, 1, 64, 128, dtype=torch.bfloat16))
+    torch.cuda.synchronize()
+    assert dit.get_device_error() == 0
