@@ -59,7 +59,7 @@ int dit_attn_version(void);
 /*
  * Prepare the current CUDA device: checks that it is compute capability 10.3,
  * reads its SM count, raises the kernels' dynamic shared-memory limit and
- * resolves the driver's tensor-map encoder.  Idempotent and thread-safe; call
+ * resolves the CUDA driver's tensor-map encoder.  Idempotent and thread-safe; call
  * once per device before dit_attn_forward.  Returns NO_DEVICE when no usable
  * device is present.
  */

@@ -9,7 +9,7 @@ call.  GPU: two calls in a row against the caller-workspace entry point (the
 same split plan and arithmetic, only the scratch address differs: bit for
 bit) and against the FP64 oracle (max|err| <= 2e-2, rel L2 <= 5e-3); no
 device memory taken by the call, neither from torch's caching allocator nor
-from the driver; NOT_INITIALIZED before dit_attn_create().
+from the CUDA driver; NOT_INITIALIZED before dit_attn_create().
 
 This file is collected last, so that a run stopping at its first failure has
 run every other test; it also passes alone in a fresh process.
@@ -108,7 +108,7 @@ def test_noalloc_large_split_workload_allocates_nothing(lib):
     for o in outs:
         lib.forward_noalloc(q, k, v, o, w.scale)
     torch.cuda.synchronize()
-    assert torch.cuda.mem_get_info()[0] == free_before     # the driver's view: nothing taken
+    assert torch.cuda.mem_get_info()[0] == free_before     # the CUDA driver's view: nothing taken
     assert torch.cuda.memory_allocated() == torch_before
     for o in outs:
         assert torch.equal(o.view(torch.int16), ref.view(torch.int16))
